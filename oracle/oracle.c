@@ -1,0 +1,450 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle of the MoE layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or constant with
+ * the CUDA library: it is an independent restatement of what the pages
+ * define, written so that a reader can check it against them line by line.
+ *
+ * What is computed, and where it is stated:
+ *   - gating, two families (softmax top-k; sigmoid scoring with a per-expert
+ *     selection bias and a routed scaling factor), plus the shared expert as
+ *     one extra slot of weight 1.0 per token:
+ *       "Distributed MoE" (tenzro docs), paragraph on the two router families;
+ *       "Expert-Sharded Swarm Inference: The Design" (kvasir), layer pseudocode;
+ *   - the dispatch plan (per-expert batches of token_indices, per-token slot
+ *     assignments): "Distributed MoE", tenzro_moePlanDispatch request and
+ *     response records;
+ *   - the expert FFN: SwiGLU over gate/up/down projections, every projection
+ *     applied as Y = X * W^T with W stored [out, in]:
+ *       "Distributed MoE", expert-host-runtime and compute-seam paragraphs;
+ *   - the combine: per-token sum of gate-weighted expert outputs plus the
+ *     shared expert: "Distributed MoE", expert-host-runtime paragraph;
+ *       "Expert-Sharded Swarm Inference: The Design", layer pseudocode;
+ *   - sharded (grouped by expert) == monolithic (per token) up to rounding:
+ *       "Expert-Sharded Swarm Inference: The Design", exactness paragraph;
+ *       "Expert-sharding" (kvasir wiki), section "Gemeten, niet beloofd".
+ *
+ * Readings taken where the pages are silent (each is listed in the design
+ * notes of the repository):
+ *   - softmax family: no renormalisation of the top-k probabilities unless
+ *     norm_topk != 0 (the pseudocode keeps softmax(...) as is);
+ *   - sigmoid family: the selection bias only chooses experts; the weights are
+ *     the unbiased sigmoid scores, divided by their sum over the selected set
+ *     when norm_topk != 0, then multiplied by routed_scaling;
+ *   - an optional per-expert logit bias lb[e] is added to the router logit
+ *     before either family's scoring (used to make skewed workloads);
+ *   - top-k ties go to the lower expert index; a token's routed slots are in
+ *     descending selection score; shared slots follow them;
+ *   - batches are in ascending expert index, token_indices ascending inside
+ *     each batch (the printed example is ascending);
+ *   - silu(z) = z / (1 + exp(-z)); SwiGLU h = silu(gate) * up.
+ *
+ * Numbers: every input is read exactly as stored (fp32 or bf16) and widened to
+ * fp64; all arithmetic is fp64.  Parallelism: OpenMP over tokens only; each
+ * token's arithmetic is the sequential loop written below.
+ */
+#include <math.h>
+#include <omp.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_F32 0
+#define OR_BF16 1
+#define OR_F64 2
+
+#define OR_GATE_SOFTMAX 0
+#define OR_GATE_SIGMOID 1
+
+#define OR_OK 0
+#define OR_EINVAL -1
+#define OR_ENOMEM -2
+#define OR_EMISSING -3
+
+/* widen element i of an fp32 / bf16 / fp64 array to double (exact) */
+static double widen(const void* p, int dt, size_t i) {
+  if (dt == OR_F32) return (double)((const float*)p)[i];
+  if (dt == OR_BF16) {
+    uint32_t bits = ((uint32_t)((const uint16_t*)p)[i]) << 16; /* bf16 = top half of fp32 */
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+  }
+  return ((const double*)p)[i];
+}
+
+/* copy n elements starting at element `off` into an fp64 row */
+static void widen_row(double* dst, const void* src, int dt, size_t off, int n) {
+  for (int i = 0; i < n; ++i) dst[i] = widen(src, dt, off + (size_t)i);
+}
+
+static double dot(const double* a, const double* b, int n) {
+  double s = 0.0;
+  for (int i = 0; i < n; ++i) s += a[i] * b[i];
+  return s;
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/* -------------------------------------------------------------------------
+ * Router: logits and selection scores of one token.
+ *   logit[e] = x_t . Wr[e] (+ lb[e])          (router weights stored [E, d])
+ *   softmax family : selection score = logit (softmax is monotone in it)
+ *   sigmoid family : selection score = sigmoid(logit) + sel_bias[e]
+ * ------------------------------------------------------------------------- */
+static void router_one(int d, int E, int gate, const double* xt, const void* Wr, int w_dt,
+                       const double* lb, const double* sb, double* logit, double* score,
+                       double* rowbuf) {
+  for (int e = 0; e < E; ++e) {
+    widen_row(rowbuf, Wr, w_dt, (size_t)e * d, d);
+    double l = dot(xt, rowbuf, d);
+    if (lb) l += lb[e];
+    logit[e] = l;
+    if (gate == OR_GATE_SOFTMAX)
+      score[e] = l;
+    else
+      score[e] = sigmoid(l) + (sb ? sb[e] : 0.0);
+  }
+}
+
+/* k largest selection scores, in descending order; ties to the lower index */
+static void topk_desc(const double* score, int E, int k, int32_t* sel, unsigned char* taken) {
+  memset(taken, 0, (size_t)E);
+  for (int j = 0; j < k; ++j) {
+    int best = -1;
+    for (int e = 0; e < E; ++e) {
+      if (taken[e]) continue;
+      if (best < 0 || score[e] > score[best]) best = e;
+    }
+    taken[best] = 1;
+    sel[j] = best;
+  }
+}
+
+/* gate weights of the selected experts */
+static void gate_weights(int E, int k, int gate, int norm_topk, double rs, const double* logit,
+                         const int32_t* sel, double* w) {
+  if (gate == OR_GATE_SOFTMAX) {
+    double m = logit[0];
+    for (int e = 1; e < E; ++e)
+      if (logit[e] > m) m = logit[e];
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) z += exp(logit[e] - m);
+    for (int j = 0; j < k; ++j) w[j] = exp(logit[sel[j]] - m) / z;
+  } else {
+    for (int j = 0; j < k; ++j) w[j] = sigmoid(logit[sel[j]]);
+  }
+  if (norm_topk) {
+    double s = 0.0;
+    for (int j = 0; j < k; ++j) s += w[j];
+    for (int j = 0; j < k; ++j) w[j] = w[j] / s;
+  }
+  for (int j = 0; j < k; ++j) w[j] = rs * w[j];
+}
+
+/* -------------------------------------------------------------------------
+ * Expert FFN of one token row:  out = Wd * (silu(Wg * v) (.) (Wu * v))
+ * Wg, Wu stored [I, d]; Wd stored [d, I]  (Y = X * W^T, W is [out, in]).
+ * ------------------------------------------------------------------------- */
+static void ffn_one(int d, int I, const double* v, const void* Wg, const void* Wu, const void* Wd,
+                    int w_dt, double* out, double* h, double* rowbuf) {
+  for (int n = 0; n < I; ++n) {
+    widen_row(rowbuf, Wg, w_dt, (size_t)n * d, d);
+    double g = dot(rowbuf, v, d);
+    widen_row(rowbuf, Wu, w_dt, (size_t)n * d, d);
+    double u = dot(rowbuf, v, d);
+    h[n] = silu(g) * u;
+  }
+  for (int m = 0; m < d; ++m) {
+    widen_row(rowbuf, Wd, w_dt, (size_t)m * I, I);
+    out[m] = dot(rowbuf, h, I);
+  }
+}
+
+static int check_common(int T, int d, int E, int k, int S, int gate) {
+  if (T < 0 || d <= 0 || E <= 0 || k <= 0 || k > E || S < 0) return OR_EINVAL;
+  if (gate != OR_GATE_SOFTMAX && gate != OR_GATE_SIGMOID) return OR_EINVAL;
+  return OR_OK;
+}
+
+static void set_threads(int nthreads) {
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+}
+
+/* Router logits and selection scores for all T tokens ([T, E] each). */
+int oracle_router_scores(int T, int d, int E, int gate, int x_dt, const void* x, int w_dt,
+                         const void* Wr, const double* lb, const double* sb, double* logits,
+                         double* scores, int nthreads) {
+  if (check_common(T, d, E, 1, 0, gate) != OR_OK) return OR_EINVAL;
+  if (gate == OR_GATE_SOFTMAX && sb) return OR_EINVAL;
+  set_threads(nthreads);
+  int err = OR_OK;
+#pragma omp parallel
+  {
+    double* xt = malloc(sizeof(double) * (size_t)d);
+    double* rowbuf = malloc(sizeof(double) * (size_t)d);
+    if (!xt || !rowbuf) {
+#pragma omp atomic write
+      err = OR_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 4)
+      for (int t = 0; t < T; ++t) {
+        widen_row(xt, x, x_dt, (size_t)t * d, d);
+        router_one(d, E, gate, xt, Wr, w_dt, lb, sb, logits + (size_t)t * E,
+                   scores + (size_t)t * E, rowbuf);
+      }
+    }
+    free(xt);
+    free(rowbuf);
+  }
+  return err;
+}
+
+/* Routing of T tokens: ids[T, k] (descending score) and gate weights w[T, k]. */
+int oracle_route(int T, int d, int E, int k, int gate, int norm_topk, double rs, int x_dt,
+                 const void* x, int w_dt, const void* Wr, const double* lb, const double* sb,
+                 int32_t* ids, double* w, int nthreads) {
+  if (check_common(T, d, E, k, 0, gate) != OR_OK) return OR_EINVAL;
+  if (gate == OR_GATE_SOFTMAX && sb) return OR_EINVAL;
+  set_threads(nthreads);
+  int err = OR_OK;
+#pragma omp parallel
+  {
+    double* xt = malloc(sizeof(double) * (size_t)d);
+    double* rowbuf = malloc(sizeof(double) * (size_t)d);
+    double* logit = malloc(sizeof(double) * (size_t)E);
+    double* score = malloc(sizeof(double) * (size_t)E);
+    unsigned char* taken = malloc((size_t)E);
+    if (!xt || !rowbuf || !logit || !score || !taken) {
+#pragma omp atomic write
+      err = OR_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 4)
+      for (int t = 0; t < T; ++t) {
+        widen_row(xt, x, x_dt, (size_t)t * d, d);
+        router_one(d, E, gate, xt, Wr, w_dt, lb, sb, logit, score, rowbuf);
+        topk_desc(score, E, k, ids + (size_t)t * k, taken);
+        gate_weights(E, k, gate, norm_topk, rs, logit, ids + (size_t)t * k, w + (size_t)t * k);
+      }
+    }
+    free(xt);
+    free(rowbuf);
+    free(logit);
+    free(score);
+    free(taken);
+  }
+  return err;
+}
+
+/* -------------------------------------------------------------------------
+ * Dispatch plan: invert token -> experts into expert -> tokens.
+ * The T*(k+S) (token, slot) pairs are visited in token-major order; slot j < k
+ * is routed expert ids[t, j], slot k + s is shared expert E + s.  Each pair
+ * lands in its expert's batch behind the earlier pairs of that expert, so
+ * token_indices are ascending inside each batch (a counting sort).
+ *   offsets[E+S+1]         : batch e is token_indices[offsets[e] .. offsets[e+1])
+ *   token_indices[T*(k+S)] : token of each batch row
+ *   slot_row[T*(k+S)]      : batch row of pair (t, j)  -- the token assignments
+ *   active_ids[E+S], n_active : experts with a non-empty batch, ascending
+ * ------------------------------------------------------------------------- */
+int oracle_plan(int T, int E, int k, int S, const int32_t* ids, int32_t* offsets,
+                int32_t* token_indices, int32_t* slot_row, int32_t* active_ids,
+                int32_t* n_active) {
+  if (T < 0 || E <= 0 || k <= 0 || S < 0) return OR_EINVAL;
+  const int nE = E + S, ks = k + S;
+  for (size_t i = 0; i < (size_t)T * k; ++i)
+    if (ids[i] < 0 || ids[i] >= E) return OR_EINVAL;
+  int64_t* count = calloc((size_t)nE, sizeof(int64_t));
+  int64_t* fill = calloc((size_t)nE, sizeof(int64_t));
+  if (!count || !fill) {
+    free(count);
+    free(fill);
+    return OR_ENOMEM;
+  }
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < ks; ++j) {
+      int e = j < k ? ids[(size_t)t * k + j] : E + (j - k);
+      count[e] += 1;
+    }
+  offsets[0] = 0;
+  for (int e = 0; e < nE; ++e) offsets[e + 1] = offsets[e] + (int32_t)count[e];
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < ks; ++j) {
+      int e = j < k ? ids[(size_t)t * k + j] : E + (j - k);
+      int32_t pos = offsets[e] + (int32_t)fill[e];
+      fill[e] += 1;
+      token_indices[pos] = t;
+      slot_row[(size_t)t * ks + j] = pos;
+    }
+  int na = 0;
+  for (int e = 0; e < nE; ++e)
+    if (count[e] > 0) active_ids[na++] = e;
+  *n_active = na;
+  free(count);
+  free(fill);
+  return OR_OK;
+}
+
+/* -------------------------------------------------------------------------
+ * Monolithic forward, token by token (the layer pseudocode):
+ *   y_t = sum_{j<k} w_tj * FFN(ids_tj, x_t) + sum_{s<S} 1.0 * FFN(E+s, x_t)
+ *         (+ residual_t when given)
+ * Only the tokens in token_list (n_list of them; all T when token_list is
+ * NULL) are computed; row i of y / ids / w belongs to token token_list[i].
+ * Expert weights come as per-expert base pointers Wg[e] ([I, d]), Wu[e]
+ * ([I, d]), Wd[e] ([d, I]) for e in 0..E+S-1; an expert that no computed
+ * token uses may be NULL.
+ * ------------------------------------------------------------------------- */
+int oracle_forward(int T, int d, int E, int k, int I, int S, int gate, int norm_topk, double rs,
+                   int x_dt, const void* x, int w_dt, const void* Wr, const double* lb,
+                   const double* sb, const void* const* Wg, const void* const* Wu,
+                   const void* const* Wd, const double* residual, int n_list,
+                   const int32_t* token_list, double* y, int32_t* ids, double* w, int nthreads) {
+  if (check_common(T, d, E, k, S, gate) != OR_OK || I <= 0) return OR_EINVAL;
+  if (gate == OR_GATE_SOFTMAX && sb) return OR_EINVAL;
+  const int n = token_list ? n_list : T;
+  for (int i = 0; i < n && token_list; ++i)
+    if (token_list[i] < 0 || token_list[i] >= T) return OR_EINVAL;
+  set_threads(nthreads);
+  int err = OR_OK;
+  const int rowlen = d > I ? d : I;
+#pragma omp parallel
+  {
+    double* xt = malloc(sizeof(double) * (size_t)d);
+    double* rowbuf = malloc(sizeof(double) * (size_t)rowlen);
+    double* logit = malloc(sizeof(double) * (size_t)E);
+    double* score = malloc(sizeof(double) * (size_t)E);
+    double* h = malloc(sizeof(double) * (size_t)I);
+    double* out = malloc(sizeof(double) * (size_t)d);
+    unsigned char* taken = malloc((size_t)E);
+    if (!xt || !rowbuf || !logit || !score || !h || !out || !taken) {
+#pragma omp atomic write
+      err = OR_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int i = 0; i < n; ++i) {
+        const int t = token_list ? token_list[i] : i;
+        int32_t* sel = ids + (size_t)i * k;
+        double* wt = w + (size_t)i * k;
+        double* yt = y + (size_t)i * d;
+        widen_row(xt, x, x_dt, (size_t)t * d, d);
+        router_one(d, E, gate, xt, Wr, w_dt, lb, sb, logit, score, rowbuf);
+        topk_desc(score, E, k, sel, taken);
+        gate_weights(E, k, gate, norm_topk, rs, logit, sel, wt);
+        for (int m = 0; m < d; ++m) yt[m] = 0.0;
+        for (int j = 0; j < k + S; ++j) {
+          const int e = j < k ? sel[j] : E + (j - k);
+          const double we = j < k ? wt[j] : 1.0;
+          if (!Wg[e] || !Wu[e] || !Wd[e]) {
+#pragma omp atomic write
+            err = OR_EMISSING;
+            continue;
+          }
+          ffn_one(d, I, xt, Wg[e], Wu[e], Wd[e], w_dt, out, h, rowbuf);
+          for (int m = 0; m < d; ++m) yt[m] += we * out[m];
+        }
+        if (residual)
+          for (int m = 0; m < d; ++m) yt[m] += residual[(size_t)t * d + m];
+      }
+    }
+    free(xt);
+    free(rowbuf);
+    free(logit);
+    free(score);
+    free(h);
+    free(out);
+    free(taken);
+  }
+  return err;
+}
+
+/* -------------------------------------------------------------------------
+ * Sharded forward: the same layer computed the way the pages' workers do it.
+ * Route every token once, build the dispatch plan, then run each expert over
+ * its batch of token rows (experts in ascending order) and add each row's
+ * gate-weighted output into its token's y.  The pages report that this
+ * regrouping equals the monolithic result up to rounding.
+ * y is [T, d]; ids / w ([T, k]) receive the routing.
+ * ------------------------------------------------------------------------- */
+int oracle_forward_sharded(int T, int d, int E, int k, int I, int S, int gate, int norm_topk,
+                           double rs, int x_dt, const void* x, int w_dt, const void* Wr,
+                           const double* lb, const double* sb, const void* const* Wg,
+                           const void* const* Wu, const void* const* Wd, const double* residual,
+                           double* y, int32_t* ids, double* w, int nthreads) {
+  if (check_common(T, d, E, k, S, gate) != OR_OK || I <= 0) return OR_EINVAL;
+  int rc = oracle_route(T, d, E, k, gate, norm_topk, rs, x_dt, x, w_dt, Wr, lb, sb, ids, w,
+                        nthreads);
+  if (rc != OR_OK) return rc;
+  const int nE = E + S, ks = k + S;
+  const size_t P = (size_t)T * ks;
+  int32_t* offsets = malloc(sizeof(int32_t) * (size_t)(nE + 1));
+  int32_t* tok = malloc(sizeof(int32_t) * (P ? P : 1));
+  int32_t* slot_row = malloc(sizeof(int32_t) * (P ? P : 1));
+  int32_t* active = malloc(sizeof(int32_t) * (size_t)nE);
+  double* wrow = malloc(sizeof(double) * (P ? P : 1));
+  int32_t na = 0;
+  if (!offsets || !tok || !slot_row || !active || !wrow) {
+    rc = OR_ENOMEM;
+    goto done;
+  }
+  rc = oracle_plan(T, E, k, S, ids, offsets, tok, slot_row, active, &na);
+  if (rc != OR_OK) goto done;
+  /* weight of each batch row: routed pair -> its gate weight, shared -> 1.0 */
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < ks; ++j)
+      wrow[slot_row[(size_t)t * ks + j]] = j < k ? w[(size_t)t * k + j] : 1.0;
+  for (size_t i = 0; i < (size_t)T * d; ++i) y[i] = 0.0;
+  set_threads(nthreads);
+  const int rowlen = d > I ? d : I;
+  for (int e = 0; e < nE && rc == OR_OK; ++e) {
+    const int32_t b0 = offsets[e], b1 = offsets[e + 1];
+    if (b1 == b0) continue;
+    if (!Wg[e] || !Wu[e] || !Wd[e]) {
+      rc = OR_EMISSING;
+      break;
+    }
+    /* rows of one batch belong to distinct tokens, so they may run in parallel */
+#pragma omp parallel
+    {
+      double* xt = malloc(sizeof(double) * (size_t)d);
+      double* rowbuf = malloc(sizeof(double) * (size_t)rowlen);
+      double* h = malloc(sizeof(double) * (size_t)I);
+      double* out = malloc(sizeof(double) * (size_t)d);
+      if (!xt || !rowbuf || !h || !out) {
+#pragma omp atomic write
+        rc = OR_ENOMEM;
+      } else {
+#pragma omp for schedule(dynamic, 1)
+        for (int32_t pos = b0; pos < b1; ++pos) {
+          const int t = tok[pos];
+          widen_row(xt, x, x_dt, (size_t)t * d, d);
+          ffn_one(d, I, xt, Wg[e], Wu[e], Wd[e], w_dt, out, h, rowbuf);
+          for (int m = 0; m < d; ++m) y[(size_t)t * d + m] += wrow[pos] * out[m];
+        }
+      }
+      free(xt);
+      free(rowbuf);
+      free(h);
+      free(out);
+    }
+  }
+  if (rc == OR_OK && residual)
+    for (size_t i = 0; i < (size_t)T * d; ++i) y[i] += residual[i];
+done:
+  free(offsets);
+  free(tok);
+  free(slot_row);
+  free(active);
+  free(wrow);
+  return rc;
+}
+
+/* Widen a whole fp32/bf16 array to fp64 (used by the tests to read stored values). */
+void oracle_widen(const void* src, int dt, size_t n, double* dst) {
+  for (size_t i = 0; i < n; ++i) dst[i] = widen(src, dt, i);
+}
+
+int oracle_max_threads(void) { return omp_get_max_threads(); }
