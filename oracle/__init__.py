@@ -12,6 +12,8 @@ Functions (each follows the passage cited in ``oracle.c``):
   plan           dispatch plan (CSR batches per expert + per-token slots)
   forward        monolithic per-token layer forward, optionally on a sample
   forward_sharded  the same layer grouped by expert (the workers' regrouping)
+  expert_rows    one expert's SwiGLU FFN over a list of token rows
+  combine        gate-weighted sum of batch rows per token plus shared rows
 """
 from __future__ import annotations
 
@@ -60,8 +62,11 @@ def _load():
     lib.oracle_forward_sharded.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, f64, i32, vp,
                                            i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32]
     lib.oracle_widen.argtypes = [vp, i32, ctypes.c_size_t, vp]
+    lib.oracle_expert_rows.argtypes = [i32, i32, i32, vp, i32, vp, vp, vp, i32, vp, vp, i32]
+    lib.oracle_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp]
     for f in ("oracle_router_scores", "oracle_route", "oracle_plan", "oracle_forward",
-              "oracle_forward_sharded", "oracle_max_threads"):
+              "oracle_forward_sharded", "oracle_max_threads", "oracle_expert_rows",
+              "oracle_combine"):
         getattr(lib, f).restype = ctypes.c_int
     lib.oracle_widen.restype = None
     _lib = lib
@@ -273,6 +278,37 @@ def forward_sharded(x, Wr, Wg, Wu, Wd, k, gate, S=0, norm_topk=0, routed_scaling
     del k1, k2, k3
     _check(rc, "oracle_forward_sharded")
     return y, ids, w
+
+
+def expert_rows(x, Wg_e, Wu_e, Wd_e, tokens, nthreads=0):
+    """FFN of one expert (weights [I, d], [I, d], [d, I]) on rows x[tokens]; [n, d] fp64."""
+    lib = _load()
+    xa, ga, ua, da = _Arr(x), _Arr(Wg_e), _Arr(Wu_e), _Arr(Wd_e)
+    if not (ga.dt == ua.dt == da.dt):
+        raise TypeError("expert weights must share one dtype")
+    d = xa.shape[1]
+    I = ga.shape[0]
+    tl = np.ascontiguousarray(tokens, dtype=np.int32)
+    out = np.empty((tl.shape[0], d), np.float64)
+    rc = lib.oracle_expert_rows(d, I, xa.dt, xa.ptr, ga.dt, ga.ptr, ua.ptr, da.ptr, tl.shape[0],
+                                tl.ctypes.data, out.ctypes.data, nthreads)
+    _check(rc, "oracle_expert_rows")
+    return out
+
+
+def combine(rows, slot_row, k, S, w=None, residual=None):
+    """y[t] = sum_j w[t, j] rows[slot_row[t, j]] + shared rows (+ residual), fp64."""
+    lib = _load()
+    rows = _f64(rows)
+    sr = np.ascontiguousarray(slot_row, dtype=np.int32)
+    T = sr.shape[0]
+    d = rows.shape[1]
+    wv, res = _f64(w), _f64(residual)
+    y = np.empty((T, d), np.float64)
+    rc = lib.oracle_combine(T, d, k, S, rows.ctypes.data, sr.ctypes.data, _ptr(wv), _ptr(res),
+                            y.ctypes.data)
+    _check(rc, "oracle_combine")
+    return y
 
 
 def widen(a):

@@ -442,6 +442,62 @@ done:
   return rc;
 }
 
+/* -------------------------------------------------------------------------
+ * One expert over a list of token rows (what a worker computes for one
+ * expert of its slice): out[i] = FFN(e, x[tokens[i]]), [n_rows, d].
+ * ------------------------------------------------------------------------- */
+int oracle_expert_rows(int d, int I, int x_dt, const void* x, int w_dt, const void* Wg,
+                       const void* Wu, const void* Wd, int n_rows, const int32_t* tokens,
+                       double* out, int nthreads) {
+  if (d <= 0 || I <= 0 || n_rows < 0 || !Wg || !Wu || !Wd) return OR_EINVAL;
+  set_threads(nthreads);
+  int err = OR_OK;
+  const int rowlen = d > I ? d : I;
+#pragma omp parallel
+  {
+    double* xt = malloc(sizeof(double) * (size_t)d);
+    double* rowbuf = malloc(sizeof(double) * (size_t)rowlen);
+    double* h = malloc(sizeof(double) * (size_t)I);
+    if (!xt || !rowbuf || !h) {
+#pragma omp atomic write
+      err = OR_ENOMEM;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int i = 0; i < n_rows; ++i) {
+        widen_row(xt, x, x_dt, (size_t)tokens[i] * d, d);
+        ffn_one(d, I, xt, Wg, Wu, Wd, w_dt, out + (size_t)i * d, h, rowbuf);
+      }
+    }
+    free(xt);
+    free(rowbuf);
+    free(h);
+  }
+  return err;
+}
+
+/* -------------------------------------------------------------------------
+ * Combine: y_t = sum_{j<k} w_tj * rows[slot_row[t, j]]
+ *                + sum_{s<S} rows[slot_row[t, k+s]]  (+ residual_t)
+ * w NULL means every routed weight is 1 (rows already weighted).
+ * ------------------------------------------------------------------------- */
+int oracle_combine(int T, int d, int k, int S, const double* rows, const int32_t* slot_row,
+                   const double* w, const double* residual, double* y) {
+  if (T < 0 || d <= 0 || k <= 0 || S < 0) return OR_EINVAL;
+  const int ks = k + S;
+  for (int t = 0; t < T; ++t) {
+    double* yt = y + (size_t)t * d;
+    for (int m = 0; m < d; ++m) yt[m] = 0.0;
+    for (int j = 0; j < ks; ++j) {
+      const int32_t r = slot_row[(size_t)t * ks + j];
+      const double wj = (j < k && w) ? w[(size_t)t * k + j] : 1.0;
+      for (int m = 0; m < d; ++m) yt[m] += wj * rows[(size_t)r * d + m];
+    }
+    if (residual)
+      for (int m = 0; m < d; ++m) yt[m] += residual[(size_t)t * d + m];
+  }
+  return OR_OK;
+}
+
 /* Widen a whole fp32/bf16 array to fp64 (used by the tests to read stored values). */
 void oracle_widen(const void* src, int dt, size_t n, double* dst) {
   for (size_t i = 0; i < n; ++i) dst[i] = widen(src, dt, i);

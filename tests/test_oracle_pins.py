@@ -396,3 +396,55 @@ def test_errors_are_reported():
         oracle.route(inp["x"], inp["Wr"], 6, oracle.GATE_SOFTMAX)
     with pytest.raises(RuntimeError):  # selection bias belongs to the sigmoid family
         oracle.route(inp["x"], inp["Wr"], 2, oracle.GATE_SOFTMAX, sel_bias=np.zeros(5))
+
+
+# ---------------------------------------------------------------- per-call pieces
+def test_expert_rows_is_swiglu_on_gathered_rows():
+    """One expert over a token list = the numpy SwiGLU MLP of the gathered rows."""
+    cfg, inp = _tiny(T=12, E=3, k=1, d=24, I=40)
+    toks = np.array([11, 0, 5, 5, 3], np.int32)
+    out = oracle.expert_rows(inp["x"], inp["Wg"][2], inp["Wu"][2], inp["Wd"][2], toks)
+    ref = _swiglu_np(_f64(inp["x"])[toks], _f64(inp["Wg"][2]), _f64(inp["Wu"][2]),
+                     _f64(inp["Wd"][2]))
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_combine_is_weighted_gather():
+    """Combine = weighted gather-sum of batch rows (numpy einsum), shared rows weight 1;
+    with k = 1, w = 1, S = 0 it is a plain row gather (exact)."""
+    rng = np.random.default_rng(12)
+    T, d, k, S = 9, 16, 3, 1
+    P = T * (k + S)
+    rows = rng.standard_normal((P, d))
+    slot_row = rng.permutation(P).astype(np.int32).reshape(T, k + S)
+    w = rng.uniform(0, 1, (T, k))
+    res = rng.standard_normal((T, d))
+    y = oracle.combine(rows, slot_row, k, S, w=w, residual=res)
+    wfull = np.concatenate([w, np.ones((T, S))], 1)
+    ref = np.einsum("tj,tjd->td", wfull, rows[slot_row]) + res
+    np.testing.assert_allclose(y, ref, rtol=1e-13, atol=1e-13)
+    sr1 = rng.permutation(T).astype(np.int32).reshape(T, 1)
+    np.testing.assert_array_equal(oracle.combine(rows[:T], sr1, 1, 0), rows[:T][sr1[:, 0]])
+    # unweighted form equals weights of one
+    np.testing.assert_allclose(oracle.combine(rows, slot_row, k, S),
+                               oracle.combine(rows, slot_row, k, S, w=np.ones((T, k))),
+                               rtol=0, atol=0)
+
+
+def test_sharded_pieces_compose_to_forward():
+    """route -> plan -> expert_rows per batch -> combine reproduces forward()."""
+    cfg, inp = _tiny(T=21, E=6, k=2, S=1, gate=oracle.GATE_SIGMOID, seed=4)
+    kw = dict(norm_topk=1, routed_scaling=2.5, sel_bias=np.linspace(-0.1, 0.1, 6))
+    y, ids, w = oracle.forward(inp["x"], inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"], 2,
+                               oracle.GATE_SIGMOID, S=1, **kw)
+    ids2, w2 = oracle.route(inp["x"], inp["Wr"], 2, oracle.GATE_SIGMOID, **kw)
+    p = oracle.plan(ids2, 6, 1)
+    off, tok = p["expert_offsets"], p["token_indices"]
+    rows = np.zeros((21 * 3, 16))
+    for e in range(7):
+        if off[e + 1] > off[e]:
+            rows[off[e]:off[e + 1]] = oracle.expert_rows(inp["x"], inp["Wg"][e], inp["Wu"][e],
+                                                         inp["Wd"][e], tok[off[e]:off[e + 1]])
+    y2 = oracle.combine(rows, p["slot_row"], 2, 1, w=w2)
+    np.testing.assert_array_equal(ids, ids2)
+    np.testing.assert_allclose(y2, y, rtol=1e-12, atol=1e-13)
