@@ -1,0 +1,386 @@
+// api.cu -- the C ABI (include/moe.h): argument checks, workspace carve-up,
+// and the stream-ordered launch sequences of the five layer calls.
+#include <math.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_desc(const moe_layer_desc* D) {
+  if (!D) return MOE_ERR_INVALID_ARG;
+  if (D->T < 0 || D->d <= 0 || D->E <= 0 || D->E > 1024 || D->k <= 0 || D->k > D->E ||
+      D->k > 32 || D->I <= 0 || D->S < 0 || D->S > 4)
+    return MOE_ERR_INVALID_ARG;
+  if (D->gate != MOE_GATE_SOFTMAX_TOPK && D->gate != MOE_GATE_SIGMOID_BIAS)
+    return MOE_ERR_INVALID_ARG;
+  if (D->norm_topk != 0 && D->norm_topk != 1) return MOE_ERR_INVALID_ARG;
+  if (!isfinite(D->routed_scaling)) return MOE_ERR_INVALID_ARG;
+  const long long P = (long long)D->T * (D->k + D->S);
+  if (P > (1ll << 30)) return MOE_ERR_UNSUPPORTED;
+  if (D->dtype == MOE_BF16) {
+    if (D->d % 64 || D->I % 64) return MOE_ERR_UNSUPPORTED;
+    const long long ng = D->E + D->S;
+    if (ng * D->I < 128 || ng * D->d < 128) return MOE_ERR_UNSUPPORTED;
+  } else if (D->dtype == MOE_F32) {
+    if (D->d % 8 || D->I % 4) return MOE_ERR_UNSUPPORTED;
+  } else {
+    return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+struct Ws {
+  int* flags;
+  float* logits;
+  int32_t* topk_ids;
+  float* topk_w;
+  int32_t* offsets;
+  int32_t* tok_idx;
+  int32_t* slot_row;
+  int32_t* active;
+  int32_t* n_active;
+  float* slot_w;
+  uint32_t* bits;
+  int32_t* wpre;
+  int32_t* counts;
+  void* x_perm;
+  void* h;
+  void* y_perm;
+};
+
+Ws carve(void* base, const WsLayout& L) {
+  uint8_t* b = static_cast<uint8_t*>(base);
+  Ws w;
+  w.flags = reinterpret_cast<int*>(b + L.flags);
+  w.logits = reinterpret_cast<float*>(b + L.logits);
+  w.topk_ids = reinterpret_cast<int32_t*>(b + L.topk_ids);
+  w.topk_w = reinterpret_cast<float*>(b + L.topk_w);
+  w.offsets = reinterpret_cast<int32_t*>(b + L.offsets);
+  w.tok_idx = reinterpret_cast<int32_t*>(b + L.tok_idx);
+  w.slot_row = reinterpret_cast<int32_t*>(b + L.slot_row);
+  w.active = reinterpret_cast<int32_t*>(b + L.active);
+  w.n_active = reinterpret_cast<int32_t*>(b + L.n_active);
+  w.slot_w = reinterpret_cast<float*>(b + L.slot_w);
+  w.bits = reinterpret_cast<uint32_t*>(b + L.plan_bits);
+  w.wpre = reinterpret_cast<int32_t*>(b + L.plan_wpre);
+  w.counts = reinterpret_cast<int32_t*>(b + L.plan_counts);
+  w.x_perm = b + L.x_perm;
+  w.h = b + L.h;
+  w.y_perm = b + L.y_perm;
+  return w;
+}
+
+moe_status check_ws(const moe_layer_desc* D, void* ws, size_t bytes) {
+  if (!ws || !aligned16(ws)) return MOE_ERR_WORKSPACE;
+  if (bytes < ws_layout(*D).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ---------------------------------------------------------------- profiling
+struct ProfRecord {
+  std::string name;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRecord> g_prof;
+std::vector<cudaEvent_t> g_prof_free;
+std::atomic<long long> g_launches{0};
+
+cudaEvent_t take_event() {
+  if (!g_prof_free.empty()) {
+    cudaEvent_t e = g_prof_free.back();
+    g_prof_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// The routing passes and the shared gating kernel.
+moe_status do_route(const moe_layer_desc* D, const void* x, const void* Wr,
+                    const float* logit_bias, const float* sel_bias, int32_t* ids, float* w,
+                    const Ws& W, cudaStream_t s) {
+  cudaError_t e = cudaErrorNotSupported;
+  if (D->dtype == MOE_BF16)
+    e = launch_router_logits_tc(x, Wr, D->T, D->d, D->E, W.logits, W.flags, s);
+  if (e == cudaErrorNotSupported)
+    e = launch_router_logits_simt(D->dtype, x, Wr, D->T, D->d, D->E, W.logits, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_router_topk(W.logits, logit_bias, sel_bias, D->T, D->E, D->k,
+                                        D->gate, D->norm_topk, D->routed_scaling, ids, w, s));
+}
+
+moe_status do_ffn(const moe_layer_desc* D, const void* x, const int32_t* offsets,
+                  const int32_t* tok_idx, const float* slot_w, const void* Wg, const void* Wu,
+                  const void* Wd, void* y_perm, const Ws& W, cudaStream_t s) {
+  const int P = D->T * (D->k + D->S);
+  const int nE = D->E + D->S;
+  cudaError_t e =
+      launch_gather_rows(D->dtype, x, tok_idx, offsets + nE, P, D->T, D->d, W.x_perm, W.flags, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (D->dtype == MOE_F32) {
+    e = launch_ffn_simt(static_cast<const float*>(W.x_perm), offsets, nE, P, D->d, D->I,
+                        static_cast<const float*>(Wg), static_cast<const float*>(Wu),
+                        static_cast<const float*>(Wd), slot_w, static_cast<float*>(W.h),
+                        static_cast<float*>(y_perm), s);
+  } else {
+    const double mean_rows = (double)P / (double)nE;
+    e = launch_ffn_tc(W.x_perm, offsets, nE, P, D->d, D->I, mean_rows, Wg, Wu, Wd, slot_w, W.h,
+                      y_perm, W.flags, s);
+  }
+  return cuda_status(e);
+}
+
+}  // namespace
+
+WsLayout ws_layout(const moe_layer_desc& D) {
+  WsLayout L{};
+  const size_t T = (size_t)D.T, E = (size_t)D.E, k = (size_t)D.k, S = (size_t)D.S;
+  const size_t nE = E + S, P = T * (k + S);
+  const size_t nw = (T + 31) / 32;
+  const size_t cap = (size_t)tc_row_capacity((int)P);
+  const size_t es = dtype_size(D.dtype);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  L.flags = take(16);
+  L.logits = take(T * E * 4);
+  L.topk_ids = take(T * k * 4);
+  L.topk_w = take(T * k * 4);
+  L.offsets = take((nE + 1) * 4);
+  L.tok_idx = take(P * 4);
+  L.slot_row = take(P * 4);
+  L.active = take(nE * 4);
+  L.n_active = take(4);
+  L.slot_w = take(P * 4);
+  L.plan_bits = take(nE * nw * 4);
+  L.plan_wpre = take(nE * nw * 4);
+  L.plan_counts = take(nE * 4);
+  L.x_perm = take(cap * (size_t)D.d * es);
+  L.h = take(cap * (size_t)D.I * es);
+  L.y_perm = take(P * (size_t)D.d * es);
+  L.total = off;
+  return L;
+}
+
+ProfScope::ProfScope(const char* n, cudaStream_t s) : name(n), stream(s), slot(-1) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  if (!g_prof_on) return;
+  ProfRecord r{n, take_event(), take_event()};
+  if (!r.start || !r.stop) return;
+  if (cudaEventRecord(r.start, s) != cudaSuccess) return;
+  g_prof.push_back(r);
+  slot = (int)g_prof.size() - 1;
+}
+
+ProfScope::~ProfScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  if (slot < (int)g_prof.size()) cudaEventRecord(g_prof[slot].stop, stream);
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int num_sms() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 64 && cache[dev]) return cache[dev];
+  int n = 1;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_workspace_size(const moe_layer_desc* desc, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  *bytes = desc->T == 0 ? 0 : ws_layout(*desc).total;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace || ws_bytes < 16 || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(workspace, 0, 16, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_route(const moe_layer_desc* desc, const void* x, const void* Wr,
+                     const float* logit_bias, const float* sel_bias, int32_t* topk_ids,
+                     float* topk_w, void* workspace, size_t ws_bytes, void* stream) {
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !Wr || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wr) || !aligned16(topk_ids) || !aligned16(topk_w))
+    return MOE_ERR_INVALID_ARG;
+  if (sel_bias && desc->gate != MOE_GATE_SIGMOID_BIAS) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
+  const Ws W = carve(workspace, ws_layout(*desc));
+  return do_route(desc, x, Wr, logit_bias, sel_bias, topk_ids, topk_w, W,
+                  static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_plan_dispatch(const moe_layer_desc* desc, const int32_t* topk_ids,
+                             const float* topk_w, int32_t* expert_offsets,
+                             int32_t* token_indices, int32_t* slot_row, int32_t* active_ids,
+                             int32_t* n_active, float* slot_w, void* workspace, size_t ws_bytes,
+                             void* stream) {
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->T == 0) return MOE_OK;
+  if (!topk_ids || !expert_offsets || !token_indices || !slot_row) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
+  const Ws W = carve(workspace, ws_layout(*desc));
+  return cuda_status(launch_plan(topk_ids, topk_w, desc->T, desc->E, desc->k, desc->S,
+                                 expert_offsets, token_indices, slot_row, active_ids, n_active,
+                                 slot_w, W.bits, W.wpre, W.counts, W.flags,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_ffn(const moe_layer_desc* desc, const void* x,
+                          const int32_t* expert_offsets, const int32_t* token_indices,
+                          const float* slot_w, const void* Wg, const void* Wu, const void* Wd,
+                          void* y_perm, void* workspace, size_t ws_bytes, void* stream) {
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !expert_offsets || !token_indices || !Wg || !Wu || !Wd || !y_perm)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) || !aligned16(y_perm))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
+  const Ws W = carve(workspace, ws_layout(*desc));
+  return do_ffn(desc, x, expert_offsets, token_indices, slot_w, Wg, Wu, Wd, y_perm, W,
+                static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_combine(const moe_layer_desc* desc, const void* y_perm, const int32_t* slot_row,
+                       const float* topk_w, const float* residual, float* y, void* stream) {
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->T == 0) return MOE_OK;
+  if (!y_perm || !slot_row || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y) || (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine(desc->dtype, y_perm, slot_row, topk_w, residual, desc->T,
+                                    desc->d, desc->k, desc->S, y,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const void* Wr,
+                             const float* logit_bias, const float* sel_bias, const void* Wg,
+                             const void* Wu, const void* Wd, const float* residual, float* y,
+                             int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !Wr || !Wg || !Wu || !Wd || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wr) || !aligned16(Wg) || !aligned16(Wu) || !aligned16(Wd) ||
+      !aligned16(y) || (residual && !aligned16(residual)) ||
+      (topk_ids_out && !aligned16(topk_ids_out)) || (topk_w_out && !aligned16(topk_w_out)))
+    return MOE_ERR_INVALID_ARG;
+  if (sel_bias && desc->gate != MOE_GATE_SIGMOID_BIAS) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Ws W = carve(workspace, ws_layout(*desc));
+  int32_t* ids = topk_ids_out ? topk_ids_out : W.topk_ids;
+  float* w = topk_w_out ? topk_w_out : W.topk_w;
+  if (cudaMemsetAsync(W.flags, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((st = do_route(desc, x, Wr, logit_bias, sel_bias, ids, w, W, s)) != MOE_OK) return st;
+  if (launch_plan(ids, nullptr, desc->T, desc->E, desc->k, desc->S, W.offsets, W.tok_idx,
+                  W.slot_row, W.active, W.n_active, nullptr, W.bits, W.wpre, W.counts, W.flags,
+                  s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((st = do_ffn(desc, x, W.offsets, W.tok_idx, nullptr, Wg, Wu, Wd, W.y_perm, W, s)) != MOE_OK)
+    return st;
+  return cuda_status(launch_combine(desc->dtype, W.y_perm, W.slot_row, w, residual, desc->T,
+                                    desc->d, desc->k, desc->S, y, s));
+}
+
+moe_status moe_get_device_status(void* workspace, size_t ws_bytes, int clear, void* stream) {
+  if (!workspace || ws_bytes < 16 || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host_flags[4] = {0, 0, 0, 0};
+  if (cudaMemcpyAsync(host_flags, workspace, sizeof(host_flags), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (clear && cudaMemsetAsync(workspace, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (host_flags[0] & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (host_flags[0] & kErrDeviceInput) return MOE_ERR_DEVICE_INPUT;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: bad pointer, size, alignment or flag";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape or dtype not supported";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing or too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call or kernel launch failed";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded wait inside a kernel expired";
+    case MOE_ERR_DEVICE_INPUT: return "MOE_ERR_DEVICE_INPUT: an input value was out of range";
+  }
+  return "unknown moe_status";
+}
+
+int64_t moe_launch_count(void) { return g_launches.load(); }
+
+moe_status moe_profile_enable(int on) {
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  for (auto& r : g_prof) {
+    g_prof_free.push_back(r.start);
+    g_prof_free.push_back(r.stop);
+  }
+  g_prof.clear();
+  g_prof_on = on != 0;
+  return MOE_OK;
+}
+
+moe_status moe_profile_query(const char* kernel, int32_t* launches, float* total_ms) {
+  if (!kernel || !launches || !total_ms) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  int n = 0;
+  float tot = 0.f;
+  for (auto& r : g_prof) {
+    if (r.name != kernel) continue;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess) return MOE_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) return MOE_ERR_CUDA;
+    tot += ms;
+    ++n;
+  }
+  *launches = n;
+  *total_ms = tot;
+  return MOE_OK;
+}
+
+}  // extern "C"

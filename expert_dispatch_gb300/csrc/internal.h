@@ -1,0 +1,91 @@
+// internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Workspace carve-up (every region 256-byte aligned).  Sizes follow the
+// layer record; P = T * (k + S) is the number of (token, slot) pairs.
+struct WsLayout {
+  size_t flags;        // int32[4]: [0] error bits, [1] plan ticket
+  size_t logits;       // fp32 [T, E]
+  size_t topk_ids;     // int32 [T, k]
+  size_t topk_w;       // fp32 [T, k]
+  size_t offsets;      // int32 [E+S+1]
+  size_t tok_idx;      // int32 [P]
+  size_t slot_row;     // int32 [P]
+  size_t active;       // int32 [E+S]
+  size_t n_active;     // int32 [1]
+  size_t slot_w;       // fp32 [P]
+  size_t plan_bits;    // uint32 [E+S, ceil(T/32)]  token bitmap per expert
+  size_t plan_wpre;    // int32 [E+S, ceil(T/32)]   popcount prefix per bitmap word
+  size_t plan_counts;  // int32 [E+S]               batch sizes
+  size_t x_perm;       // dtype [cap, d], cap = tc_row_capacity(P)
+  size_t h;            // dtype [cap, I]
+  size_t y_perm;       // dtype [P, d]
+  size_t total;
+};
+
+WsLayout ws_layout(const moe_layer_desc& d);
+
+// Rows of the permuted-row buffers for P batch rows (see tc_gemm.cu).
+int tc_row_capacity(int P);
+
+inline size_t dtype_size(int dt) { return dt == MOE_BF16 ? 2 : 4; }
+
+// ---------------------------------------------------------------- profiling hooks
+struct ProfScope {
+  ProfScope(const char* name, cudaStream_t s);
+  ~ProfScope();
+  const char* name;
+  cudaStream_t stream;
+  int slot;
+};
+void count_launch();
+
+// ---------------------------------------------------------------- launchers
+// Each returns cudaSuccess or the launch error.
+
+// logits[T, E] = x[T, d] * Wr[E, d]^T (+ logit_bias), fp32 accumulate, CUDA cores.
+cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, int T, int d,
+                                      int E, float* logits, cudaStream_t s);
+// tcgen05 version (bf16); returns cudaErrorNotSupported when the shape does not fit.
+cudaError_t launch_router_logits_tc(const void* x, const void* Wr, int T, int d, int E,
+                                    float* logits, int* err, cudaStream_t s);
+// per-token top-k and gate weights from logits
+cudaError_t launch_router_topk(const float* logits, const float* logit_bias,
+                               const float* sel_bias, int T, int E, int k, int gate,
+                               int norm_topk, float rs, int32_t* ids, float* w, cudaStream_t s);
+
+cudaError_t launch_plan(const int32_t* ids, const float* topk_w, int T, int E, int k, int S,
+                        int32_t* offsets, int32_t* tok_idx, int32_t* slot_row, int32_t* active,
+                        int32_t* n_active, float* slot_w, uint32_t* bits, int32_t* wpre,
+                        int32_t* counts, int* flags, cudaStream_t s);
+
+cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* tok_idx,
+                               const int32_t* total_rows, int P, int T, int d, void* x_perm,
+                               int* flags, cudaStream_t s);
+
+// fp32 SIMT expert FFN: h = silu(x_perm Wg^T) * (x_perm Wu^T); y_perm = (h Wd^T) * slot_w
+cudaError_t launch_ffn_simt(const float* x_perm, const int32_t* offsets, int n_groups, int P,
+                            int d, int I, const float* Wg, const float* Wu, const float* Wd,
+                            const float* slot_w, float* h, float* y_perm, cudaStream_t s);
+
+// bf16 tcgen05 expert FFN (gate/up + SwiGLU, then down)
+cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_groups, int P,
+                          int d, int I, double mean_rows, const void* Wg, const void* Wu,
+                          const void* Wd, const float* slot_w, void* h, void* y_perm, int* err,
+                          cudaStream_t s);
+
+cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_row,
+                           const float* topk_w, const float* residual, int T, int d, int k,
+                           int S, float* y, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace moe

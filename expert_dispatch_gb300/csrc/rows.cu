@@ -1,0 +1,127 @@
+// rows.cu -- row movement around the expert FFN.
+//
+// gather_rows : x_perm[r] = x[token_indices[r]] for every batch row r, so
+//               that each expert's batch is a contiguous block of rows (the
+//               "send (cur rows, local_ids) to the worker" step of the layer
+//               pseudocode in "Expert-Sharded Swarm Inference: The Design",
+//               done as an in-HBM permutation).
+// combine     : y[t] = sum_{j<k} w[t,j] * y_perm[slot_row[t,j]]
+//                      + sum_{s<S} y_perm[slot_row[t,k+s]] (+ residual[t]),
+//               in that fixed order, fp32 ("Distributed MoE" (tenzro docs),
+//               expert-host-runtime paragraph: outputs recombined weighted by
+//               the gate probabilities; the shared expert is one more slot
+//               of weight 1.0 -- router-families paragraph).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+// One warp per row, 16-byte vectors.  Rows at or beyond *total_rows are
+// unused capacity and skipped; a token index outside [0, T) is flagged and
+// its row left untouched.
+__global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ tok,
+                                   const int32_t* __restrict__ total_rows, int P, int T,
+                                   int vec_per_row, uint4* __restrict__ x_perm, int* flags) {
+  const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= P || r >= *total_rows) return;
+  const int t = tok[r];
+  if (t < 0 || t >= T) {
+    if (lane == 0) flag_error(flags, kErrDeviceInput);
+    return;
+  }
+  const uint4* src = x + (size_t)t * vec_per_row;
+  uint4* dst = x_perm + (size_t)r * vec_per_row;
+  for (int v = lane; v < vec_per_row; v += 32) dst[v] = src[v];
+}
+
+__device__ __forceinline__ void add8(float (&acc)[8], uint4 v, float w) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+    acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+  }
+}
+
+// One block per token; each thread owns 8 consecutive columns per pass.
+template <bool BF16>
+__global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ y_perm,
+                                                      const int32_t* __restrict__ slot_row,
+                                                      const float* __restrict__ topk_w,
+                                                      const float* __restrict__ residual, int d,
+                                                      int k, int S, int P,
+                                                      float* __restrict__ y) {
+  const int t = blockIdx.x;
+  const int ks = k + S;
+  const int32_t* sr = slot_row + (size_t)t * ks;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < ks; ++j) {
+      const int r = sr[j];
+      if (r < 0 || r >= P) continue;  // dropped pair (or a row outside the batch rows)
+      const float w = (j < k && topk_w) ? topk_w[(size_t)t * k + j] : 1.f;
+      if (BF16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(y_perm) + (size_t)r * d + c);
+        add8(acc, v, w);
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(
+            static_cast<const float*>(y_perm) + (size_t)r * d + c);
+        const float4 a = src[0], b = src[1];
+        acc[0] = fmaf(w, a.x, acc[0]);
+        acc[1] = fmaf(w, a.y, acc[1]);
+        acc[2] = fmaf(w, a.z, acc[2]);
+        acc[3] = fmaf(w, a.w, acc[3]);
+        acc[4] = fmaf(w, b.x, acc[4]);
+        acc[5] = fmaf(w, b.y, acc[5]);
+        acc[6] = fmaf(w, b.z, acc[6]);
+        acc[7] = fmaf(w, b.w, acc[7]);
+      }
+    }
+    if (residual) {
+      const float4* rs = reinterpret_cast<const float4*>(residual + (size_t)t * d + c);
+      const float4 a = rs[0], b = rs[1];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    float4* dst = reinterpret_cast<float4*>(y + (size_t)t * d + c);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* tok_idx,
+                               const int32_t* total_rows, int P, int T, int d, void* x_perm,
+                               int* flags, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  const int vec = (int)(d * dtype_size(dtype) / 16);
+  ProfScope pr("gather_rows", s);
+  count_launch();
+  gather_rows_kernel<<<(P + 7) / 8, 256, 0, s>>>(static_cast<const uint4*>(x), tok_idx,
+                                                 total_rows, P, T, vec,
+                                                 static_cast<uint4*>(x_perm), flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_row,
+                           const float* topk_w, const float* residual, int T, int d, int k,
+                           int S, float* y, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int P = T * (k + S);
+  ProfScope pr("combine", s);
+  count_launch();
+  if (dtype == MOE_BF16)
+    combine_kernel<true><<<T, 128, 0, s>>>(y_perm, slot_row, topk_w, residual, d, k, S, P, y);
+  else
+    combine_kernel<false><<<T, 128, 0, s>>>(y_perm, slot_row, topk_w, residual, d, k, S, P, y);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,294 @@
+"""Thin Python binding of libmoe.so (include/moe.h).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Tensors are torch tensors (PyTorch supplies device memory and
+streams); each function checks device, dtype, shape and contiguity, passes raw
+pointers and the current CUDA stream, and raises ``MoeError`` on a non-OK
+status.  There is no fallback: if libmoe.so is missing, every call raises.
+
+Entry points carry the C names: moe_workspace_size, moe_workspace_init,
+moe_route, moe_plan_dispatch, moe_expert_ffn, moe_combine, moe_layer_forward,
+moe_get_device_status, moe_status_string, moe_launch_count,
+moe_profile_enable, moe_profile_query.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_DEVICE_INPUT = 6
+
+MOE_GATE_SOFTMAX_TOPK = 0
+MOE_GATE_SIGMOID_BIAS = 1
+MOE_F32 = 0
+MOE_BF16 = 1
+
+EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_dispatch",
+            "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status",
+            "moe_status_string", "moe_launch_count", "moe_profile_enable", "moe_profile_query")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s: %s" % (what, moe_status_string(status)))
+
+
+class LayerDesc(ctypes.Structure):
+    """moe_layer_desc"""
+    _fields_ = [("layer", ctypes.c_int32), ("T", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("S", ctypes.c_int32), ("gate", ctypes.c_int32), ("norm_topk", ctypes.c_int32),
+                ("routed_scaling", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+def make_desc(T, d, E, k, I, S=0, gate=MOE_GATE_SOFTMAX_TOPK, norm_topk=0, routed_scaling=1.0,
+              dtype=MOE_BF16, layer=0) -> LayerDesc:
+    return LayerDesc(layer, T, d, E, k, I, S, gate, norm_topk, routed_scaling, dtype)
+
+
+def desc_from_config(cfg, T=None) -> LayerDesc:
+    """Layer record of a workload config (expert_dispatch_gb300.inputs.LayerConfig)."""
+    return make_desc(cfg.T if T is None else T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.S, cfg.gate,
+                     cfg.norm_topk, cfg.routed_scaling,
+                     MOE_F32 if cfg.dtype == "f32" else MOE_BF16)
+
+
+_lib = None
+
+
+def lib():
+    """Open libmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libmoe.so is not built (run python -m expert_dispatch_gb300.build); "
+                           "this package has no fallback path")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    D = ctypes.POINTER(LayerDesc)
+    L.moe_workspace_size.argtypes = [D, ctypes.POINTER(sz)]
+    L.moe_workspace_init.argtypes = [vp, sz, vp]
+    L.moe_route.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_plan_dispatch.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_expert_ffn.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_combine.argtypes = [D, vp, vp, vp, vp, vp, vp]
+    L.moe_layer_forward.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_get_device_status.argtypes = [vp, sz, i32, vp]
+    L.moe_status_string.argtypes = [i32]
+    L.moe_status_string.restype = ctypes.c_char_p
+    L.moe_launch_count.argtypes = []
+    L.moe_launch_count.restype = ctypes.c_int64
+    L.moe_profile_enable.argtypes = [i32]
+    L.moe_profile_query.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
+                                    ctypes.POINTER(ctypes.c_float)]
+    for f in EXPORTED:
+        if f not in ("moe_status_string", "moe_launch_count"):
+            getattr(L, f).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+# ---------------------------------------------------------------- marshalling helpers
+def _p(t, dtype=None, what="tensor"):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % what)
+    if t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (what, dtype, t.dtype))
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _act_dtype(desc):
+    return torch.float32 if desc.dtype == MOE_F32 else torch.bfloat16
+
+
+def _check(status, what):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def _need(t, shape, what):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (what, tuple(t.shape), tuple(shape)))
+
+
+# ---------------------------------------------------------------- entry points
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def moe_workspace_size(desc: LayerDesc) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(ctypes.byref(desc), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def alloc_workspace(desc: LayerDesc, device="cuda") -> torch.Tensor:
+    """A uint8 device buffer of moe_workspace_size(desc) bytes, flag cleared."""
+    ws = torch.empty(max(moe_workspace_size(desc), 256), dtype=torch.uint8, device=device)
+    moe_workspace_init(ws)
+    return ws
+
+
+def moe_workspace_init(ws, stream=None):
+    _check(lib().moe_workspace_init(_p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)),
+           "moe_workspace_init")
+
+
+def moe_route(desc, x, Wr, logit_bias, sel_bias, topk_ids, topk_w, ws, stream=None):
+    dt = _act_dtype(desc)
+    _need(x, (desc.T, desc.d), "x")
+    _need(Wr, (desc.E, desc.d), "Wr")
+    _need(topk_ids, (desc.T, desc.k), "topk_ids")
+    _need(topk_w, (desc.T, desc.k), "topk_w")
+    st = lib().moe_route(ctypes.byref(desc), _p(x, dt, "x"), _p(Wr, dt, "Wr"),
+                         _p(logit_bias, torch.float32, "logit_bias"),
+                         _p(sel_bias, torch.float32, "sel_bias"),
+                         _p(topk_ids, torch.int32, "topk_ids"), _p(topk_w, torch.float32, "topk_w"),
+                         _p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream))
+    _check(st, "moe_route")
+
+
+def moe_plan_dispatch(desc, topk_ids, topk_w, expert_offsets, token_indices, slot_row,
+                      active_ids, n_active, slot_w, ws, stream=None):
+    P = desc.T * (desc.k + desc.S)
+    _need(topk_ids, (desc.T, desc.k), "topk_ids")
+    _need(expert_offsets, (desc.E + desc.S + 1,), "expert_offsets")
+    _need(token_indices, (P,), "token_indices")
+    _need(slot_row, (desc.T, desc.k + desc.S), "slot_row")
+    st = lib().moe_plan_dispatch(
+        ctypes.byref(desc), _p(topk_ids, torch.int32, "topk_ids"),
+        _p(topk_w, torch.float32, "topk_w"), _p(expert_offsets, torch.int32, "expert_offsets"),
+        _p(token_indices, torch.int32, "token_indices"), _p(slot_row, torch.int32, "slot_row"),
+        _p(active_ids, torch.int32, "active_ids"), _p(n_active, torch.int32, "n_active"),
+        _p(slot_w, torch.float32, "slot_w"), _p(ws, torch.uint8, "workspace"), ws.numel(),
+        _stream(stream))
+    _check(st, "moe_plan_dispatch")
+
+
+def moe_expert_ffn(desc, x, expert_offsets, token_indices, slot_w, Wg, Wu, Wd, y_perm, ws,
+                   stream=None):
+    dt = _act_dtype(desc)
+    nE = desc.E + desc.S
+    _need(x, (desc.T, desc.d), "x")
+    _need(Wg, (nE, desc.I, desc.d), "Wg")
+    _need(Wu, (nE, desc.I, desc.d), "Wu")
+    _need(Wd, (nE, desc.d, desc.I), "Wd")
+    _need(y_perm, (desc.T * (desc.k + desc.S), desc.d), "y_perm")
+    st = lib().moe_expert_ffn(
+        ctypes.byref(desc), _p(x, dt, "x"), _p(expert_offsets, torch.int32, "expert_offsets"),
+        _p(token_indices, torch.int32, "token_indices"), _p(slot_w, torch.float32, "slot_w"),
+        _p(Wg, dt, "Wg"), _p(Wu, dt, "Wu"), _p(Wd, dt, "Wd"), _p(y_perm, dt, "y_perm"),
+        _p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream))
+    _check(st, "moe_expert_ffn")
+
+
+def moe_combine(desc, y_perm, slot_row, topk_w, residual, y, stream=None):
+    dt = _act_dtype(desc)
+    _need(y_perm, (desc.T * (desc.k + desc.S), desc.d), "y_perm")
+    _need(slot_row, (desc.T, desc.k + desc.S), "slot_row")
+    _need(y, (desc.T, desc.d), "y")
+    st = lib().moe_combine(ctypes.byref(desc), _p(y_perm, dt, "y_perm"),
+                           _p(slot_row, torch.int32, "slot_row"),
+                           _p(topk_w, torch.float32, "topk_w"),
+                           _p(residual, torch.float32, "residual"), _p(y, torch.float32, "y"),
+                           _stream(stream))
+    _check(st, "moe_combine")
+
+
+def moe_layer_forward(desc, x, Wr, logit_bias, sel_bias, Wg, Wu, Wd, residual, y, topk_ids_out,
+                      topk_w_out, ws, stream=None):
+    dt = _act_dtype(desc)
+    nE = desc.E + desc.S
+    _need(x, (desc.T, desc.d), "x")
+    _need(Wr, (desc.E, desc.d), "Wr")
+    _need(Wg, (nE, desc.I, desc.d), "Wg")
+    _need(Wu, (nE, desc.I, desc.d), "Wu")
+    _need(Wd, (nE, desc.d, desc.I), "Wd")
+    _need(y, (desc.T, desc.d), "y")
+    st = lib().moe_layer_forward(
+        ctypes.byref(desc), _p(x, dt, "x"), _p(Wr, dt, "Wr"),
+        _p(logit_bias, torch.float32, "logit_bias"), _p(sel_bias, torch.float32, "sel_bias"),
+        _p(Wg, dt, "Wg"), _p(Wu, dt, "Wu"), _p(Wd, dt, "Wd"),
+        _p(residual, torch.float32, "residual"), _p(y, torch.float32, "y"),
+        _p(topk_ids_out, torch.int32, "topk_ids_out"), _p(topk_w_out, torch.float32, "topk_w_out"),
+        _p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream))
+    _check(st, "moe_layer_forward")
+
+
+def moe_get_device_status(ws, clear=False, stream=None) -> int:
+    """Synchronizes the stream and returns the workspace's sticky device status."""
+    return lib().moe_get_device_status(_p(ws, torch.uint8, "workspace"), ws.numel(),
+                                       1 if clear else 0, _stream(stream))
+
+
+def moe_launch_count() -> int:
+    return lib().moe_launch_count()
+
+
+def moe_profile_enable(on: bool):
+    _check(lib().moe_profile_enable(1 if on else 0), "moe_profile_enable")
+
+
+def moe_profile_query(kernel: str):
+    """(launches, total_ms) recorded for one kernel name since profiling was enabled."""
+    n = ctypes.c_int32(0)
+    ms = ctypes.c_float(0.0)
+    _check(lib().moe_profile_query(kernel.encode(), ctypes.byref(n), ctypes.byref(ms)),
+           "moe_profile_query")
+    return n.value, ms.value
+
+
+# ---------------------------------------------------------------- convenience
+class MoeLayer:
+    """A layer's weights and workspace on the device, with a forward() that calls
+    moe_layer_forward.  Weights are used in place (no copies)."""
+
+    def __init__(self, desc: LayerDesc, Wr, Wg, Wu, Wd, logit_bias=None, sel_bias=None):
+        self.desc = desc
+        self.Wr, self.Wg, self.Wu, self.Wd = Wr, Wg, Wu, Wd
+        self.logit_bias, self.sel_bias = logit_bias, sel_bias
+        self.ws = alloc_workspace(desc, device=Wr.device)
+
+    def forward(self, x, residual=None, y=None, topk_ids=None, topk_w=None, stream=None):
+        d = self.desc
+        if y is None:
+            y = torch.empty((d.T, d.d), dtype=torch.float32, device=x.device)
+        moe_layer_forward(d, x, self.Wr, self.logit_bias, self.sel_bias, self.Wg, self.Wu,
+                          self.Wd, residual, y, topk_ids, topk_w, self.ws, stream)
+        return y
+
+    def forward_host(self, x_host, y_host, x_dev, y_dev, stream=None):
+        """End-to-end call with host buffers: pinned x_host -> device, the layer,
+        device y -> pinned y_host (all on one stream, asynchronous)."""
+        s = stream if stream is not None else torch.cuda.current_stream()
+        with torch.cuda.stream(s):
+            x_dev.copy_(x_host, non_blocking=True)
+            self.forward(x_dev, y=y_dev, stream=s)
+            y_host.copy_(y_dev, non_blocking=True)
+        return y_host

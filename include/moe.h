@@ -1,0 +1,200 @@
+/*
+ * moe.h -- C ABI of the GB300 MoE expert-parallel layer forward (libmoe.so).
+ *
+ * The layer the pages describe, on one GPU:
+ *   route          gate a batch of hidden states, top-k          (moe_route)
+ *   plan dispatch  group token rows per expert into batches      (moe_plan_dispatch)
+ *   expert FFN     run every batch through its SwiGLU expert     (moe_expert_ffn)
+ *   combine        gate-weighted sum + shared expert (+residual) (moe_combine)
+ *   layer forward  all four in one stream-ordered sequence       (moe_layer_forward)
+ * Sources: "Distributed MoE" (tenzro docs) -- the RPC list (route, execute,
+ * forward), the tenzro_moePlanDispatch records, the router-families and
+ * expert-host-runtime paragraphs; "Expert-Sharded Swarm Inference: The Design"
+ * (kvasir) -- the layer pseudocode; "Expert-sharding" (kvasir wiki), section
+ * "Twee rollen" -- the worker request (n_used, n_tokens, cur, sel).
+ *
+ * Conventions for every call
+ *   - Pointers are DEVICE pointers unless stated otherwise; the caller owns every
+ *     buffer.  The library allocates no device memory: scratch comes from the
+ *     caller's workspace, sized by moe_workspace_size().
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Every call is asynchronous and stream-ordered; no call synchronizes the
+ *     device except moe_get_device_status().  The calls can be captured in a
+ *     CUDA graph.
+ *   - Argument errors are returned synchronously, before anything is launched.
+ *     A failed launch returns MOE_ERR_CUDA.  Problems only the device can see
+ *     (an expert id out of range, a bounded wait that expired) set a sticky
+ *     flag in the workspace that moe_get_device_status() reports.  No exception
+ *     or abort crosses the ABI.
+ *   - T = 0 is a valid no-op (MOE_OK, nothing launched).
+ *   - All pointers must be 16-byte aligned; row-major tensors are contiguous.
+ *
+ * Layouts (row-major; the expert index is the outermost dimension, so each
+ * expert's weights are one contiguous slab -- "Expert-Sharded Swarm Inference:
+ * The Design", slicing paragraph; projections are Y = X * W^T with W stored
+ * [out, in] -- "Distributed MoE", compute-seam paragraph):
+ *   x        [T, d]          dtype                 hidden states (already normed)
+ *   Wr       [E, d]          dtype                 router
+ *   Wg, Wu   [E+S, I, d]     dtype                 gate / up projections
+ *   Wd       [E+S, d, I]     dtype                 down projection
+ *   experts 0..E-1 are routed, E..E+S-1 are the shared experts.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or flag */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid but not supported (see constraints) */
+  MOE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait inside a kernel expired */
+  MOE_ERR_DEVICE_INPUT = 6  /* device: an input value was out of range (e.g. expert id) */
+} moe_status;
+
+/* Gating families ("Distributed MoE", router-families paragraph). */
+typedef enum {
+  /* Qwen layout: w = softmax(logits)[top-k of logits]; renormalised over the
+     top-k only when norm_topk != 0; times routed_scaling (1.0 normally). */
+  MOE_GATE_SOFTMAX_TOPK = 0,
+  /* DeepSeek / Kimi layout: s = sigmoid(logits); the top-k of s + sel_bias is
+     selected; w = s[sel] (divided by its sum over the selection when
+     norm_topk != 0) times routed_scaling.  The bias only selects. */
+  MOE_GATE_SIGMOID_BIAS = 1
+} moe_gate_kind;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+/* The self-describing layer record: shapes plus gating metadata
+   ("Distributed MoE", router-families paragraph: the gate blob carries its
+   bias and scaling metadata). */
+typedef struct {
+  int32_t layer;           /* carried for the caller's bookkeeping; not used */
+  int32_t T;               /* tokens in the batch (>= 0) */
+  int32_t d;               /* hidden size */
+  int32_t E;               /* routed experts */
+  int32_t k;               /* experts per token, 1 <= k <= min(E, 32) */
+  int32_t I;               /* SwiGLU intermediate size (routed and shared) */
+  int32_t S;               /* shared experts, 0 <= S <= 4, weight 1.0 each */
+  int32_t gate;            /* moe_gate_kind */
+  int32_t norm_topk;       /* 0 / 1 */
+  float routed_scaling;    /* multiplies the routed gate weights */
+  int32_t dtype;           /* moe_dtype of x and of every weight */
+} moe_layer_desc;
+
+/* Constraints: dtype MOE_BF16 needs d % 64 == 0 and I % 64 == 0 (tensor-core
+   path) and (E+S) * min(d, I) >= 128; MOE_F32 needs d % 8 == 0 and
+   I % 4 == 0.  E <= 1024, T * (k + S) <= 2^30.  Violations return
+   MOE_ERR_UNSUPPORTED.  Routing ids handed to moe_plan_dispatch must be
+   distinct within a token (as any top-k is). */
+
+/* Bytes of workspace any call below needs for this layer (0 when T == 0).
+   The same buffer may be reused by every call on the same stream. */
+moe_status moe_workspace_size(const moe_layer_desc* desc, size_t* bytes);
+
+/* Clears the workspace's device-status flag (asynchronously, on `stream`).
+   moe_layer_forward clears it itself; call this once on a fresh workspace
+   before using the individual calls with moe_get_device_status(). */
+moe_status moe_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/* moe_route -- gate a batch ("Distributed MoE", RPC list: route; layer
+   pseudocode: ids, p = top_k(softmax(cur @ router), k)).
+     logit_bias [E] fp32 or NULL: added to every token's router logits
+                 (a per-expert logit offset, both families).
+     sel_bias   [E] fp32 or NULL: selection bias, sigmoid family only
+                 (MOE_ERR_INVALID_ARG with the softmax family).
+     topk_ids   [T, k] int32 out: descending selection score, ties to the
+                 lower expert index.
+     topk_w     [T, k] fp32 out: gate weights of those experts.            */
+moe_status moe_route(const moe_layer_desc* desc, const void* x, const void* Wr,
+                     const float* logit_bias, const float* sel_bias, int32_t* topk_ids,
+                     float* topk_w, void* workspace, size_t ws_bytes, void* stream);
+
+/* moe_plan_dispatch -- invert the routing into per-expert batches
+   ("Distributed MoE", tenzro_moePlanDispatch records: batches of
+   token_indices per (layer, expert) and per-token slot assignments).
+   Pairs (t, j), j < k routed (expert topk_ids[t, j]) and j = k + s shared
+   (expert E + s), are placed by a stable counting sort in token-major order:
+     expert_offsets [E+S+1] int32 out: batch e = rows offsets[e] .. offsets[e+1]
+     token_indices  [T*(k+S)] int32 out: token of each batch row, ascending
+                    inside every batch
+     slot_row       [T, k+S] int32 out: batch row of pair (t, j) (the token
+                    assignments; token_indices[slot_row[t, j]] == t)
+     active_ids     [E+S] int32 out (or NULL): experts with a non-empty batch,
+                    ascending; n_active [1] int32 out (or NULL) their count.
+     topk_w         [T, k] fp32 in (or NULL), slot_w [T*(k+S)] fp32 out (or
+                    NULL): the gate weight of every batch row (1.0 for shared
+                    rows), for moe_expert_ffn's optional row scaling.
+   An id outside [0, E) sets MOE_ERR_DEVICE_INPUT in the workspace flag; that
+   pair is dropped (slot_row = -1) and nothing is written out of bounds.     */
+moe_status moe_plan_dispatch(const moe_layer_desc* desc, const int32_t* topk_ids,
+                             const float* topk_w, int32_t* expert_offsets,
+                             int32_t* token_indices, int32_t* slot_row, int32_t* active_ids,
+                             int32_t* n_active, float* slot_w, void* workspace, size_t ws_bytes,
+                             void* stream);
+
+/* moe_expert_ffn -- run every batch through its expert ("Distributed MoE",
+   RPC list: execute; expert-host-runtime paragraph: SwiGLU over gate/up/down;
+   "Expert-sharding", section "Twee rollen": the worker's three mat-muls):
+     y_perm[r] = slot_w[r] * Wd_e (silu(Wg_e x_t) * (Wu_e x_t)),
+   for every batch row r of expert e with token t = token_indices[r];
+   slot_w NULL means a factor of 1.  y_perm is [T*(k+S), d] in the layer's
+   dtype (bf16 rows for MOE_BF16, fp32 for MOE_F32).                      */
+moe_status moe_expert_ffn(const moe_layer_desc* desc, const void* x,
+                          const int32_t* expert_offsets, const int32_t* token_indices,
+                          const float* slot_w, const void* Wg, const void* Wu, const void* Wd,
+                          void* y_perm, void* workspace, size_t ws_bytes, void* stream);
+
+/* moe_combine -- gate-weighted sum per token plus the shared experts
+   ("Distributed MoE", expert-host-runtime paragraph: recombine weighted by
+   the gate probabilities; layer pseudocode: combine(p, partials) + shared):
+     y[t] = sum_{j<k} topk_w[t, j] * y_perm[slot_row[t, j]]
+            + sum_{s<S} y_perm[slot_row[t, k+s]]  (+ residual[t])
+   summed in that fixed order in fp32.  topk_w NULL means the rows are
+   already weighted (moe_expert_ffn with slot_w).  residual [T, d] fp32 or
+   NULL; y [T, d] fp32 out.  Rows whose slot_row is -1 are skipped.        */
+moe_status moe_combine(const moe_layer_desc* desc, const void* y_perm, const int32_t* slot_row,
+                       const float* topk_w, const float* residual, float* y, void* stream);
+
+/* moe_layer_forward -- gate -> plan -> expert FFN -> combine ("Distributed
+   MoE", RPC list: forward).  topk_ids_out [T, k] / topk_w_out [T, k] may be
+   NULL; everything else as in the calls above.                             */
+moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const void* Wr,
+                             const float* logit_bias, const float* sel_bias, const void* Wg,
+                             const void* Wu, const void* Wd, const float* residual, float* y,
+                             int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                             size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream`, then reports the sticky device flag held in the
+   workspace: MOE_OK, MOE_ERR_DEVICE_INPUT or MOE_ERR_TIMEOUT (MOE_ERR_CUDA if
+   the copy itself fails).  clear != 0 resets the flag afterwards.          */
+moe_status moe_get_device_status(void* workspace, size_t ws_bytes, int clear, void* stream);
+
+/* Human-readable name of a status; never NULL. */
+const char* moe_status_string(moe_status status);
+
+/* Kernel launches made by this library since it was loaded (all threads). */
+int64_t moe_launch_count(void);
+
+/* Profiling.  moe_profile_enable(1) starts recording a CUDA event pair around
+   every kernel this library launches (on the launching stream) and clears
+   earlier records; moe_profile_enable(0) stops.  moe_profile_query()
+   synchronizes on the recorded events and returns, for the named kernel, the
+   number of recorded launches and their summed device time in milliseconds.
+   Kernel names: router_logits_simt, router_logits_tc, router_topk,
+   plan_mark, plan_scan, plan_place, gather_rows, ffn_gateup_simt,
+   ffn_down_simt, ffn_gateup_tc, ffn_down_tc, combine.                      */
+moe_status moe_profile_enable(int on);
+moe_status moe_profile_query(const char* kernel, int32_t* launches, float* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

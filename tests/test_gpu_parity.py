@@ -1,0 +1,295 @@
+"""GPU parity: every C-ABI call against the fp64 oracle on the same seeded inputs.
+
+Routing (ids) and the dispatch plan must match bit-exactly; gate weights within
+the fp32-accumulation bound; layer outputs within max|dy|/max|y| <= 1e-5 (fp32
+layer) or 1e-2 (bf16 layer).  Small cases span several tiles and ragged tails;
+the five workloads run at full size with sampled tokens checked one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from expert_dispatch_gb300 import moe
+from expert_dispatch_gb300.inputs import (CONFIGS, DECODE_TS, KIMI_DECODE, LayerConfig,
+                                          make_inputs)
+from tests.helpers import W_RTOL, enforce_margins, host, rel_err, y_tol
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from expert_dispatch_gb300 import build
+    build.build()
+    yield
+    torch.cuda.synchronize()
+
+
+def _case(cfg, seed=0):
+    inp = make_inputs(cfg, seed=seed, device=DEV)
+    return enforce_margins(inp, cfg, seed)
+
+
+def _oracle_kw(cfg, inp):
+    return dict(norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling,
+                logit_bias=host(inp["logit_bias"]), sel_bias=host(inp["sel_bias"]))
+
+
+def _gpu_layer(cfg, inp, residual=None):
+    desc = moe.desc_from_config(cfg)
+    ws = moe.alloc_workspace(desc)
+    y = torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.float32, device=DEV)
+    ids = torch.full((cfg.T, cfg.k), -7, dtype=torch.int32, device=DEV)
+    w = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
+    moe.moe_layer_forward(desc, inp["x"], inp["Wr"], inp["logit_bias"], inp["sel_bias"],
+                          inp["Wg"], inp["Wu"], inp["Wd"], residual, y, ids, w, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    return y, ids, w, ws
+
+
+def _experts_on_host(inp, needed, nE):
+    lists = []
+    for name in ("Wg", "Wu", "Wd"):
+        W = inp[name]
+        lists.append([host(W[e]) if e in needed else None for e in range(nE)])
+    return lists
+
+
+def _oracle_forward(cfg, inp, tokens, ids_ref, residual=None):
+    needed = set(np.unique(ids_ref[tokens]).tolist()) | set(range(cfg.E, cfg.E + cfg.S))
+    Wg, Wu, Wd = _experts_on_host(inp, needed, cfg.E + cfg.S)
+    y, ids, w = oracle.forward(host(inp["x"]), host(inp["Wr"]), Wg, Wu, Wd, cfg.k, cfg.gate,
+                               S=cfg.S, residual=host(residual), tokens=tokens,
+                               **_oracle_kw(cfg, inp))
+    return y, ids, w
+
+
+# ---------------------------------------------------------------- router
+ROUTER_CASES = [
+    LayerConfig("r_fp32", T=64, d=256, E=16, I=128, k=2, dtype="f32"),
+    LayerConfig("r_bf16_simt", T=45, d=128, E=40, I=64, k=6, S=1, gate=1, norm_topk=1,
+                routed_scaling=2.5, sel_bias_range=0.1),
+    LayerConfig("r_bf16_tc", T=300, d=192, E=130, I=64, k=8, zipf_s=1.2),
+    LayerConfig("r_bf16_tc_sig", T=517, d=256, E=256, I=64, k=8, S=1, gate=1, norm_topk=1,
+                routed_scaling=2.827, sel_bias_range=0.1),
+]
+
+
+@pytest.mark.parametrize("cfg", ROUTER_CASES, ids=lambda c: c.name)
+def test_route_parity(cfg):
+    inp = _case(cfg, seed=3)
+    desc = moe.desc_from_config(cfg)
+    ws = moe.alloc_workspace(desc)
+    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    w = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
+    moe.moe_route(desc, inp["x"], inp["Wr"], inp["logit_bias"], inp["sel_bias"], ids, w, ws)
+    ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
+                                  **_oracle_kw(cfg, inp))
+    np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
+    np.testing.assert_allclose(host(w).numpy(), w_ref, rtol=W_RTOL, atol=0)
+
+
+# ---------------------------------------------------------------- planner
+PLAN_CASES = [(1, 4, 2, 0), (5, 8, 3, 1), (33, 40, 8, 0), (1000, 256, 8, 1), (4099, 64, 6, 2),
+              (2, 1024, 32, 0)]
+
+
+def _random_ids(T, E, k, seed):
+    rng = np.random.default_rng(seed)
+    ids = np.empty((T, k), np.int32)
+    for t in range(T):
+        ids[t] = rng.choice(E, size=k, replace=False)
+    return ids
+
+
+@pytest.mark.parametrize("T,E,k,S", PLAN_CASES)
+def test_plan_parity(T, E, k, S):
+    ids = _random_ids(T, E, k, seed=T + E)
+    w = np.random.default_rng(1).uniform(0, 1, (T, k)).astype(np.float32)
+    desc = moe.make_desc(T, 64, E, k, 64, S, dtype=moe.MOE_BF16)
+    ws = moe.alloc_workspace(desc)
+    P = T * (k + S)
+    g_ids = torch.from_numpy(ids).to(DEV)
+    g_w = torch.from_numpy(w).to(DEV)
+    off = torch.full((E + S + 1,), -1, dtype=torch.int32, device=DEV)
+    tok = torch.full((P,), -1, dtype=torch.int32, device=DEV)
+    sr = torch.full((T, k + S), -1, dtype=torch.int32, device=DEV)
+    act = torch.full((E + S,), -1, dtype=torch.int32, device=DEV)
+    na = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    sw = torch.zeros((P,), dtype=torch.float32, device=DEV)
+    for _ in range(2):  # a second call on the same workspace gives the same plan
+        moe.moe_plan_dispatch(desc, g_ids, g_w, off, tok, sr, act, na, sw, ws)
+        assert moe.moe_get_device_status(ws) == moe.MOE_OK
+        ref = oracle.plan(ids, E, S)
+        np.testing.assert_array_equal(host(off).numpy(), ref["expert_offsets"])
+        np.testing.assert_array_equal(host(tok).numpy(), ref["token_indices"])
+        np.testing.assert_array_equal(host(sr).numpy(), ref["slot_row"])
+        n = int(host(na)[0])
+        assert n == ref["n_active"]
+        np.testing.assert_array_equal(host(act).numpy()[:n], ref["active_ids"])
+    # slot weights follow the rows: routed pairs carry their gate weight, shared rows 1.0
+    wfull = np.concatenate([w, np.ones((T, S), np.float32)], 1)
+    exp = np.empty(P, np.float32)
+    exp[ref["slot_row"].ravel()] = wfull.ravel()
+    np.testing.assert_array_equal(host(sw).numpy(), exp)
+
+
+def test_plan_flags_out_of_range_ids():
+    T, E, k = 6, 8, 2
+    ids = _random_ids(T, E, k, 5)
+    ids[2, 1] = E + 3
+    ids[4, 0] = -1
+    desc = moe.make_desc(T, 64, E, k, 64, 0, dtype=moe.MOE_BF16)
+    ws = moe.alloc_workspace(desc)
+    off = torch.empty((E + 1,), dtype=torch.int32, device=DEV)
+    tok = torch.empty((T * k,), dtype=torch.int32, device=DEV)
+    sr = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    moe.moe_plan_dispatch(desc, torch.from_numpy(ids).to(DEV), None, off, tok, sr, None, None,
+                          None, ws)
+    assert moe.moe_get_device_status(ws, clear=True) == moe.MOE_ERR_DEVICE_INPUT
+    s = host(sr).numpy()
+    assert s[2, 1] == -1 and s[4, 0] == -1
+    assert int(host(off)[-1]) == T * k - 2  # the bad pairs are dropped
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK  # cleared
+
+
+# ---------------------------------------------------------------- expert FFN
+FFN_CASES = [
+    LayerConfig("f_fp32", T=64, d=256, E=16, I=128, k=2, dtype="f32"),
+    LayerConfig("f_fp32_ragged", T=37, d=72, E=5, I=36, k=3, S=1, dtype="f32", gate=1,
+                norm_topk=1, routed_scaling=2.0, sel_bias_range=0.1),
+    LayerConfig("f_bf16_small_tiles", T=67, d=128, E=8, I=192, k=2, S=1, gate=1, norm_topk=1,
+                routed_scaling=2.5, sel_bias_range=0.1),
+    LayerConfig("f_bf16_large_tiles", T=600, d=256, E=4, I=320, k=2),
+    LayerConfig("f_bf16_skewed", T=700, d=192, E=12, I=128, k=3, zipf_s=1.2),
+    LayerConfig("f_bf16_one_token", T=1, d=512, E=32, I=256, k=4, S=1, gate=1, norm_topk=1,
+                routed_scaling=2.8, sel_bias_range=0.1),
+]
+
+
+@pytest.mark.parametrize("cfg", FFN_CASES, ids=lambda c: c.name)
+def test_expert_ffn_and_combine_parity(cfg):
+    inp = _case(cfg, seed=5)
+    ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
+                                  **_oracle_kw(cfg, inp))
+    ref = oracle.plan(ids_ref, cfg.E, cfg.S)
+    desc = moe.desc_from_config(cfg)
+    ws = moe.alloc_workspace(desc)
+    P = cfg.T * (cfg.k + cfg.S)
+    off = torch.from_numpy(ref["expert_offsets"]).to(DEV)
+    tok = torch.from_numpy(ref["token_indices"]).to(DEV)
+    y_perm = torch.zeros((P, cfg.d), dtype=cfg.torch_dtype, device=DEV)
+    moe.moe_expert_ffn(desc, inp["x"], off, tok, None, inp["Wg"], inp["Wu"], inp["Wd"], y_perm,
+                       ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    # oracle: each batch through its expert
+    x_h = host(inp["x"])
+    rows = np.zeros((P, cfg.d))
+    o = ref["expert_offsets"]
+    for e in range(cfg.E + cfg.S):
+        if o[e + 1] > o[e]:
+            rows[o[e]:o[e + 1]] = oracle.expert_rows(x_h, host(inp["Wg"][e]), host(inp["Wu"][e]),
+                                                     host(inp["Wd"][e]), ref["token_indices"][o[e]:o[e + 1]])
+    got = host(y_perm).double().numpy()
+    assert rel_err(got, rows) <= y_tol(cfg), rel_err(got, rows)
+    # per-expert check too: no batch may be silently wrong inside the global max
+    for e in range(cfg.E + cfg.S):
+        if o[e + 1] > o[e]:
+            assert rel_err(got[o[e]:o[e + 1]], rows[o[e]:o[e + 1]]) <= 4 * y_tol(cfg)
+    # combine of the GPU rows against the oracle combine of the same rows
+    res = torch.randn((cfg.T, cfg.d), generator=torch.Generator(device=DEV).manual_seed(2),
+                      device=DEV)
+    g_w = torch.from_numpy(w_ref.astype(np.float32)).to(DEV)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=DEV)
+    sr = torch.from_numpy(ref["slot_row"]).to(DEV)
+    moe.moe_combine(desc, y_perm, sr, g_w, res, y)
+    ref_y = oracle.combine(got, ref["slot_row"], cfg.k, cfg.S, w=w_ref.astype(np.float32),
+                           residual=host(res))
+    assert rel_err(host(y).numpy(), ref_y) <= 1e-6
+
+
+# ---------------------------------------------------------------- whole layer, small
+LAYER_CASES = FFN_CASES + [ROUTER_CASES[2], ROUTER_CASES[3]]
+
+
+@pytest.mark.parametrize("cfg", LAYER_CASES, ids=lambda c: c.name)
+def test_layer_forward_parity_small(cfg):
+    inp = _case(cfg, seed=7)
+    residual = torch.randn((cfg.T, cfg.d), generator=torch.Generator(device=DEV).manual_seed(9),
+                           device=DEV)
+    y, ids, w, _ = _gpu_layer(cfg, inp, residual=residual)
+    ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
+                                  **_oracle_kw(cfg, inp))
+    np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
+    np.testing.assert_allclose(host(w).numpy(), w_ref, rtol=W_RTOL, atol=0)
+    y_ref, _, _ = _oracle_forward(cfg, inp, np.arange(cfg.T, dtype=np.int32), ids_ref,
+                                  residual=residual)
+    # the residual is exact in fp32; compare the MoE part against its own scale
+    moe_part = host(y).double().numpy() - host(residual).double().numpy()
+    moe_ref = y_ref - host(residual).double().numpy()
+    assert rel_err(moe_part, moe_ref) <= y_tol(cfg), rel_err(moe_part, moe_ref)
+
+
+def test_layer_forward_is_deterministic():
+    cfg = FFN_CASES[4]
+    inp = _case(cfg, seed=11)
+    y1, ids1, w1, _ = _gpu_layer(cfg, inp)
+    y2, ids2, w2, _ = _gpu_layer(cfg, inp)
+    assert torch.equal(ids1, ids2) and torch.equal(w1, w2) and torch.equal(y1, y2)
+
+
+# ---------------------------------------------------------------- the five workloads, full size
+def _full_size(cfg, n_sample, seed=0):
+    inp = _case(cfg, seed=seed)
+    y, ids, w, ws = _gpu_layer(cfg, inp)
+    ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
+                                  **_oracle_kw(cfg, inp))
+    np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
+    np.testing.assert_allclose(host(w).numpy(), w_ref, rtol=W_RTOL, atol=0)
+    # the plan of the full routing, bit-exact
+    desc = moe.desc_from_config(cfg)
+    P = cfg.T * (cfg.k + cfg.S)
+    off = torch.empty((cfg.E + cfg.S + 1,), dtype=torch.int32, device=DEV)
+    tok = torch.empty((P,), dtype=torch.int32, device=DEV)
+    sr = torch.empty((cfg.T, cfg.k + cfg.S), dtype=torch.int32, device=DEV)
+    moe.moe_plan_dispatch(desc, ids, None, off, tok, sr, None, None, None, ws)
+    ref = oracle.plan(ids_ref, cfg.E, cfg.S)
+    np.testing.assert_array_equal(host(off).numpy(), ref["expert_offsets"])
+    np.testing.assert_array_equal(host(tok).numpy(), ref["token_indices"])
+    np.testing.assert_array_equal(host(sr).numpy(), ref["slot_row"])
+    # sampled tokens through the oracle, one by one
+    rng = np.random.default_rng(seed)
+    n = min(n_sample, cfg.T)
+    tokens = np.sort(rng.choice(cfg.T, size=n, replace=False)).astype(np.int32)
+    y_ref, _, _ = _oracle_forward(cfg, inp, tokens, ids_ref)
+    got = host(y[torch.from_numpy(tokens).long().to(DEV)]).double().numpy()
+    assert np.isfinite(host(y).numpy()).all()
+    err = rel_err(got, y_ref)
+    assert err <= y_tol(cfg), err
+    del inp, y, ws
+    torch.cuda.empty_cache()
+
+
+def test_full_tiny_fp32():
+    _full_size(CONFIGS["tiny_fp32"], n_sample=64)
+
+
+def test_full_qwen_t512():
+    _full_size(CONFIGS["qwen_t512"], n_sample=48)
+
+
+def test_full_deepseek_prefill():
+    _full_size(CONFIGS["deepseek_prefill"], n_sample=8)
+
+
+def test_full_skewed_zipf():
+    _full_size(CONFIGS["skewed_zipf"], n_sample=24)
+
+
+@pytest.mark.parametrize("T", DECODE_TS)
+def test_full_kimi_decode(T):
+    _full_size(KIMI_DECODE.with_T(T), n_sample=8)
