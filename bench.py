@@ -1,0 +1,414 @@
+"""Benchmark of the MoE layer forward on GB300: tokens/s and % of roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one moe_layer_forward (route -> plan -> expert FFN -> combine) over
+one batch of synthetic tokens.  The default workload is the Qwen-layout batch
+(T=512, d=4096, E=256, I=1536, softmax top-8, bf16 weights).  Under torchrun
+every rank runs its own replica on its own GPU (weak scaling, no data-path
+collective); the timed region is bracketed by a barrier and a synchronize and
+the slowest rank's time counts.  Rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle (the deliberately slow reference)
+on a bounded sample of the same workload on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from expert_dispatch_gb300 import moe  # noqa: E402
+from expert_dispatch_gb300.inputs import CONFIGS, KIMI_DECODE, make_inputs  # noqa: E402
+
+METRIC = "MoE layer tokens/s on 1 GB300 (prefill + decode) and % of tensor/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PUBLISHED_CONTEXT = ("53k tok/s per worker at batch 512 on ROCm hardware, expert shape and "
+                     "precision unstated (context only, not the same workload)")
+KERNELS = ("router_logits_simt", "router_logits_tc", "router_topk", "plan_mark", "plan_scan",
+           "plan_place", "gather_rows", "ffn_gateup_simt", "ffn_down_simt", "ffn_gateup_tc",
+           "ffn_down_tc", "combine")
+
+
+def workload(name, T=None, E=None):
+    """A named workload; T / E override its batch size / expert count (small
+    profiling cases of the same layer shape)."""
+    if name.startswith("kimi_decode"):
+        cfg = KIMI_DECODE.with_T(int(name.split("@T")[1]) if "@T" in name else 1)
+    else:
+        cfg = CONFIGS[name]
+    if T is not None or E is not None:
+        cfg = dataclasses.replace(cfg, T=T or cfg.T, E=E or cfg.E,
+                                  name="%s@T%d@E%d" % (cfg.name.split("@")[0], T or cfg.T,
+                                                       E or cfg.E))
+    return cfg
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks sampling
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.5)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, on):
+        if on:
+            self.t_on = time.time()
+        else:
+            self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [r for (t, r) in self.rows if self.t_on <= t <= self.t_off + 0.1]
+        if not inside:  # very short region: the nearest samples
+            inside = [r for (t, r) in self.rows][-3:]
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in inside:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- algorithmic work
+def layer_work(cfg, n_active_routed):
+    """F (flop) and B (bytes) of one layer call, per the hot-path scope table:
+    router + expert flops; active weights + router + x + fp32 y bytes."""
+    P = cfg.T * cfg.k
+    bw = bx = 2 if cfg.dtype == "bf16" else 4
+    F = 2.0 * cfg.T * cfg.d * cfg.E + 6.0 * cfg.d * cfg.I * (P + cfg.S * cfg.T)
+    B = ((n_active_routed * 3 * cfg.d * cfg.I + cfg.S * 3 * cfg.d * cfg.I) * bw
+         + cfg.E * cfg.d * bw + cfg.T * cfg.d * bx + cfg.T * cfg.d * 4)
+    return F, B
+
+
+def kernel_bytes(cfg, kernel, n_active_all):
+    """Algorithmic bytes of one launch: the weights of every active expert it
+    streams plus the rows it must read and write once."""
+    P = cfg.T * (cfg.k + cfg.S)
+    es = 2 if cfg.dtype == "bf16" else 4
+    if kernel in ("ffn_gateup_tc", "ffn_gateup_simt"):
+        return n_active_all * 2 * cfg.I * cfg.d * es + P * cfg.d * es + P * cfg.I * es
+    if kernel in ("ffn_down_tc", "ffn_down_simt"):
+        return n_active_all * cfg.d * cfg.I * es + P * cfg.I * es + P * cfg.d * es
+    return None
+
+
+def traffic_record(kernel, cfg):
+    """dram bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel source and this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        recs = json.load(f)
+    src = os.path.join(ROOT, "expert_dispatch_gb300", "csrc", "tc_gemm.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for r in recs:
+        if r.get("kernel") == kernel and r.get("workload") == cfg.name and r.get("source") == sha:
+            return r.get("bytes_per_launch")
+    return None
+
+
+# ---------------------------------------------------------------- the GPU arm
+def run_gpu(args, rank, world):
+    cfg = workload(args.workload, args.T, args.E)
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from expert_dispatch_gb300 import build
+    if rank == 0 or not os.path.exists(moe.LIB_PATH):
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    inp = make_inputs(cfg, seed=args.seed + rank, device=dev)
+    desc = moe.desc_from_config(cfg)
+    layer = moe.MoeLayer(desc, inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"],
+                         logit_bias=inp["logit_bias"], sel_bias=inp["sel_bias"])
+    x = inp["x"]
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
+    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        layer.forward(x, y=y, topk_ids=ids, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if moe.moe_get_device_status(layer.ws) != moe.MOE_OK:
+        raise RuntimeError("device status not OK after warm-up")
+    n_active_routed = int(torch.unique(ids).numel())
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    # ---- timed region (device time, CUDA events on the launching stream)
+    moe.moe_profile_enable(True)
+    launches0 = moe.moe_launch_count()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(False)
+    if world > 1:
+        torch.distributed.barrier()
+    launches = moe.moe_launch_count() - launches0
+    ms = e0.elapsed_time(e1)
+    per_kernel = {}
+    for kname in KERNELS:
+        n, tot = moe.moe_profile_query(kname)
+        if n:
+            per_kernel[kname] = {"launches": n, "ms_per_launch": tot / n, "share": None}
+    moe.moe_profile_enable(False)
+    clocks = sampler.stop() if sampler else None
+    if moe.moe_get_device_status(layer.ws) != moe.MOE_OK:
+        raise RuntimeError("device status not OK after the timed region")
+
+    # ---- end to end: pinned host x -> device, layer, device y -> pinned host
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(x)
+    for _ in range(max(1, args.warmup)):
+        layer.forward_host(x_host, y_host, x_dev, y, stream=stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        layer.forward_host(x_host, y_host, x_dev, y, stream=stream)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    tokens = cfg.T * args.steps * world
+    value = tokens / (ms / 1e3)
+    pk, src = peaks()
+    F, B = layer_work(cfg, n_active_routed)
+    step_s = ms / 1e3 / args.steps
+    t_star = max(F / (pk["bf16_tflops"] * 1e12), B / (pk["hbm_gbs"] * 1e9))
+    total_kernel_ms = sum(v["ms_per_launch"] * v["launches"] for v in per_kernel.values())
+    for v in per_kernel.values():
+        v["share"] = v["ms_per_launch"] * v["launches"] / total_kernel_ms if total_kernel_ms else None
+    n_active_all = n_active_routed + cfg.S
+    cands = [k for k in per_kernel if kernel_bytes(cfg, k, n_active_all)]
+    dom = max(cands, key=lambda k: per_kernel[k]["ms_per_launch"] * per_kernel[k]["launches"])
+    dom_bytes = kernel_bytes(cfg, dom, n_active_all)
+    achieved = dom_bytes / (per_kernel[dom]["ms_per_launch"] / 1e3) / 1e9
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+        "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "I": cfg.I,
+                   "k": cfg.k, "shared": cfg.S,
+                   "gate": "softmax" if cfg.gate == 0 else "sigmoid+bias",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: each step streams %.1f GB of expert weights"
+                         % (B / 1e9)},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved,
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "traffic": traffic_record(dom, cfg),
+                     "algorithmic_bytes_per_launch": dom_bytes, "peak_source": src},
+        "layer_roofline": {"flop": F, "bytes": B, "n_active_experts": n_active_routed,
+                           "t_star_ms": t_star * 1e3, "frac": t_star / step_s,
+                           "tc_frac": F / step_s / (pk["bf16_tflops"] * 1e12),
+                           "hbm_frac": B / step_s / (pk["hbm_gbs"] * 1e9), "peak_source": src},
+        "kernels": per_kernel,
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "published_context": PUBLISHED_CONTEXT,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg, inp, budget_s=args.cpu_budget)
+    return out
+
+
+# ---------------------------------------------------------------- the oracle (CPU)
+def _oracle_inputs(cfg, inp):
+    return {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+
+
+def oracle_time(cfg, host, n_tokens, seed=0):
+    import numpy as np
+
+    import oracle
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(cfg.T, size=n_tokens, replace=False)).astype(np.int32)
+    t0 = time.perf_counter()
+    oracle.forward(host["x"], host["Wr"], host["Wg"], host["Wu"], host["Wd"], cfg.k, cfg.gate,
+                   S=cfg.S, norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling,
+                   logit_bias=host["logit_bias"], sel_bias=host["sel_bias"], tokens=toks)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, inp, budget_s=10.0):
+    """The oracle as it stands, on this machine's cores, over a bounded token sample."""
+    import oracle
+    host = _oracle_inputs(cfg, inp)
+    cores = oracle.max_threads()
+    n0 = min(cfg.T, max(1, cores))
+    t0 = oracle_time(cfg, host, n0)
+    n = int(min(cfg.T, max(n0, n0 * budget_s / max(t0, 1e-3))))
+    t = oracle_time(cfg, host, n, seed=1) if n > n0 else t0
+    return {"value": n / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "%d of the workload's %d tokens through the fp64 oracle (%.1f s)"
+                      % (n, cfg.T, t)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    cfg = workload(args.workload, args.T, args.E)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = make_inputs(cfg, seed=args.seed, device=dev)  # the same tensors the GPU arm uses
+    host = _oracle_inputs(cfg, inp)
+    del inp
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    # size one step's sample so that warm-up + steps finish in a few minutes
+    n_cal = min(cfg.T, max(1, cores))
+    t_cal = oracle_time(cfg, host, n_cal)
+    per_tok = t_cal / n_cal
+    per_step_budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))
+    n = int(min(cfg.T, max(1, per_step_budget / per_tok)))
+    for i in range(args.warmup):
+        oracle_time(cfg, host, n, seed=100 + i)
+    times = [oracle_time(cfg, host, n, seed=i) for i in range(args.steps)]
+    total = sum(times)
+    value = n * args.steps / total
+    return {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+        "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "I": cfg.I,
+                   "k": cfg.k, "shared": cfg.S},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": "%d of the workload's %d tokens per step" % (n, cfg.T)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="qwen_t512",
+                    help="tiny_fp32 | qwen_t512 | deepseek_prefill | skewed_zipf | "
+                         "kimi_decode@T{1,8,32,64}")
+    ap.add_argument("--T", type=int, default=None, help="override the workload's tokens")
+    ap.add_argument("--E", type=int, default=None, help="override the workload's experts")
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3  # the timing rules want at least three untimed steps
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        torch.distributed.init_process_group("nccl")
+    try:
+        out = run_reference(args, rank, world) if args.impl == "reference" else \
+            run_gpu(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+    finally:
+        if world > 1 and args.impl == "ours":
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
