@@ -36,7 +36,8 @@ MOE_BF16 = 1
 
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status",
-            "moe_status_string", "moe_launch_count", "moe_profile_enable", "moe_profile_query")
+            "moe_status_string", "moe_launch_count", "moe_profile_enable", "moe_profile_query",
+            "moe_expert_ffn_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -91,6 +92,7 @@ def lib():
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_launch_count.argtypes = []
     L.moe_launch_count.restype = ctypes.c_int64
+    L.moe_expert_ffn_noalloc.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_profile_enable.argtypes = [i32]
     L.moe_profile_query.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
                                     ctypes.POINTER(ctypes.c_float)]
@@ -206,6 +208,28 @@ def moe_expert_ffn(desc, x, expert_offsets, token_indices, slot_w, Wg, Wu, Wd, y
         _p(Wg, dt, "Wg"), _p(Wu, dt, "Wu"), _p(Wd, dt, "Wd"), _p(y_perm, dt, "y_perm"),
         _p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream))
     _check(st, "moe_expert_ffn")
+
+
+def moe_expert_ffn_noalloc(desc, x, expert_offsets, token_indices, slot_w, Wg, Wu, Wd, y_perm,
+                           stream=None):
+    """moe_expert_ffn without a workspace, for callers that cannot allocate device
+    memory (their host application owns it all, or they must never call cudaMalloc).
+    The scratch is a fixed 64 MiB array inside the library, shared by every call on
+    a device: calls must not overlap on the GPU.  Larger layers raise
+    MoeError(MOE_ERR_UNSUPPORTED)."""
+    dt = _act_dtype(desc)
+    nE = desc.E + desc.S
+    _need(x, (desc.T, desc.d), "x")
+    _need(Wg, (nE, desc.I, desc.d), "Wg")
+    _need(Wu, (nE, desc.I, desc.d), "Wu")
+    _need(Wd, (nE, desc.d, desc.I), "Wd")
+    _need(y_perm, (desc.T * (desc.k + desc.S), desc.d), "y_perm")
+    st = lib().moe_expert_ffn_noalloc(
+        ctypes.byref(desc), _p(x, dt, "x"), _p(expert_offsets, torch.int32, "expert_offsets"),
+        _p(token_indices, torch.int32, "token_indices"), _p(slot_w, torch.float32, "slot_w"),
+        _p(Wg, dt, "Wg"), _p(Wu, dt, "Wu"), _p(Wd, dt, "Wd"), _p(y_perm, dt, "y_perm"),
+        _stream(stream))
+    _check(st, "moe_expert_ffn_noalloc")
 
 
 def moe_combine(desc, y_perm, slot_row, topk_w, residual, y, stream=None):

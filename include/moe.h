@@ -152,6 +152,31 @@ moe_status moe_expert_ffn(const moe_layer_desc* desc, const void* x,
                           const float* slot_w, const void* Wg, const void* Wu, const void* Wd,
                           void* y_perm, void* workspace, size_t ws_bytes, void* stream);
 
+/* moe_expert_ffn_noalloc -- moe_expert_ffn for callers that cannot allocate
+   device memory.  The pages have no counterpart to this call; it exists for
+   callers that cannot lend the library a workspace: code inside a host
+   application that owns all device memory through its own allocator and
+   offers no way to get more, or latency-critical code that must never call
+   cudaMalloc (which may synchronize the device).  Inputs, outputs and results
+   are those of moe_expert_ffn; the scratch (gathered rows and the SwiGLU
+   intermediate) lives in a fixed 64 MiB array inside the library instead:
+     - a layer needing more (256 B + two buffers of round32(T*(k+S)) + 256 rows
+       of d and of I elements) returns MOE_ERR_UNSUPPORTED, launching nothing;
+     - every GPU that loads the library's device code holds the array until
+       the process exits;
+     - all calls on a device share the array and it keeps the last call's
+       contents: calls that overlap on the GPU race, so the caller must order
+       them (one stream, or explicit dependencies);
+     - the first call on each device looks up the array's address with that
+       device current; make that first call before any stream capture;
+     - device-detected problems (bad token indices, timeouts) are not reported
+       by this call; use moe_expert_ffn with a workspace to see them.
+   Nothing is allocated: no cudaMalloc, cudaFree or allocating library call. */
+moe_status moe_expert_ffn_noalloc(const moe_layer_desc* desc, const void* x,
+                                  const int32_t* expert_offsets, const int32_t* token_indices,
+                                  const float* slot_w, const void* Wg, const void* Wu,
+                                  const void* Wd, void* y_perm, void* stream);
+
 /* moe_combine -- gate-weighted sum per token plus the shared experts
    ("Distributed MoE", expert-host-runtime paragraph: recombine weighted by
    the gate probabilities; layer pseudocode: combine(p, partials) + shared):
