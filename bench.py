@@ -39,8 +39,8 @@ METRIC = "MoE layer tokens/s on 1 GB300 (prefill + decode) and % of tensor/HBM r
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PUBLISHED_CONTEXT = ("53k tok/s per worker at batch 512 on ROCm hardware, expert shape and "
                      "precision unstated (context only, not the same workload)")
-KERNELS = ("router_logits_simt", "router_logits_tc", "router_topk", "plan_mark", "plan_scan",
-           "plan_place", "gather_rows", "ffn_gateup_simt", "ffn_down_simt", "ffn_gateup_tc",
+KERNELS = ("router_logits_splitk", "router_logits_tc", "router_topk", "plan_small", "plan_mark",
+           "plan_scan", "plan_place", "gather_rows", "ffn_gateup_simt", "ffn_down_simt", "ffn_gateup_tc",
            "ffn_down_tc", "combine")
 
 
@@ -193,23 +193,38 @@ def run_gpu(args, rank, world):
     x = inp["x"]
     y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
     ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()
 
-    def step():
-        layer.forward(x, y=y, topk_ids=ids, stream=stream)
+    def step():  # one layer forward on the current stream
+        layer.forward(x, y=y, topk_ids=ids)
 
-    for _ in range(args.warmup):
-        step()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
     torch.cuda.synchronize()
     if moe.moe_get_device_status(layer.ws) != moe.MOE_OK:
         raise RuntimeError("device status not OK after warm-up")
     n_active_routed = int(torch.unique(ids).numel())
 
+    # The layer has fixed shapes, so a step is captured once as a CUDA graph
+    # (the library's launches are stream-ordered and allocation-free) and
+    # replayed; --no-graph times plain launches instead.
+    graph = None
+    kernels_per_step = None
+    if args.graph:
+        c0 = moe.moe_launch_count()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        kernels_per_step = moe.moe_launch_count() - c0
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
     # ---- timed region (device time, CUDA events on the launching stream)
-    moe.moe_profile_enable(True)
     launches0 = moe.moe_launch_count()
     if world > 1:
         torch.distributed.barrier()
@@ -218,26 +233,40 @@ def run_gpu(args, rank, world):
         sampler.mark(True)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+        e1.record(stream)
     torch.cuda.synchronize()
     if sampler:
         sampler.mark(False)
     if world > 1:
         torch.distributed.barrier()
-    launches = moe.moe_launch_count() - launches0
+    launches = (kernels_per_step * args.steps if graph is not None
+                else moe.moe_launch_count() - launches0)
     ms = e0.elapsed_time(e1)
+    clocks = sampler.stop() if sampler else None
+    if moe.moe_get_device_status(layer.ws) != moe.MOE_OK:
+        raise RuntimeError("device status not OK after the timed region")
+
+    # ---- per-kernel device times: the same K steps launched directly, with an
+    # event pair recorded around every library launch on the launching stream
+    moe.moe_profile_enable(True)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            step()
+    torch.cuda.synchronize()
     per_kernel = {}
     for kname in KERNELS:
         n, tot = moe.moe_profile_query(kname)
         if n:
             per_kernel[kname] = {"launches": n, "ms_per_launch": tot / n, "share": None}
     moe.moe_profile_enable(False)
-    clocks = sampler.stop() if sampler else None
-    if moe.moe_get_device_status(layer.ws) != moe.MOE_OK:
-        raise RuntimeError("device status not OK after the timed region")
+    stream = torch.cuda.current_stream()
 
     # ---- end to end: pinned host x -> device, layer, device y -> pinned host
     x_host = x.cpu().pin_memory()
@@ -302,6 +331,8 @@ def run_gpu(args, rank, world):
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
         "gpu_launches": launches,
+        "launch_mode": "cuda_graph_replay" if graph is not None else "direct",
+        "kernel_timing": "event pair per launch over %d directly launched steps" % args.steps,
         "clocks": clocks,
         "published_context": PUBLISHED_CONTEXT,
     }
@@ -393,6 +424,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", dest="graph", action="store_false",
+                    help="time direct launches instead of CUDA-graph replays")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3  # the timing rules want at least three untimed steps

@@ -117,14 +117,16 @@ cudaEvent_t take_event() {
 moe_status do_route(const moe_layer_desc* D, const void* x, const void* Wr,
                     const float* logit_bias, const float* sel_bias, int32_t* ids, float* w,
                     const Ws& W, cudaStream_t s) {
-  cudaError_t e = cudaErrorNotSupported;
-  if (D->dtype == MOE_BF16)
-    e = launch_router_logits_tc(x, Wr, D->T, D->d, D->E, W.logits, W.flags, s);
-  if (e == cudaErrorNotSupported)
-    e = launch_router_logits_simt(D->dtype, x, Wr, D->T, D->d, D->E, W.logits, s);
+  const RouterPlan rp = router_plan(D->dtype, D->T, D->d, D->E);
+  const cudaError_t e =
+      rp.tc ? launch_router_logits_tc(x, Wr, D->T, D->d, D->E, rp.ksplit, rp.kb_per, W.logits,
+                                      W.flags, s)
+            : launch_router_logits_splitk(D->dtype, x, Wr, D->T, D->d, D->E, rp.kc, rp.ksplit,
+                                          W.logits, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_router_topk(W.logits, logit_bias, sel_bias, D->T, D->E, D->k,
-                                        D->gate, D->norm_topk, D->routed_scaling, ids, w, s));
+  return cuda_status(launch_router_topk(W.logits, rp.ksplit, logit_bias, sel_bias, D->T, D->E,
+                                        D->k, D->gate, D->norm_topk, D->routed_scaling, ids, w,
+                                        s));
 }
 
 moe_status do_ffn(const moe_layer_desc* D, const void* x, const int32_t* offsets,
@@ -150,6 +152,27 @@ moe_status do_ffn(const moe_layer_desc* D, const void* x, const int32_t* offsets
 
 }  // namespace
 
+RouterPlan router_plan(int dtype, int T, int d, int E) {
+  RouterPlan r{};
+  if (dtype == MOE_BF16 && T >= 32 && E >= 128) {
+    // enough units (128 experts x 128 tokens x K chunk) for ~2 per SM, at most 16 chunks
+    r.tc = 1;
+    const int KB = d / 64;
+    const int base = ((E + 127) / 128) * ((T + 127) / 128);
+    int ks = (296 + base - 1) / base;
+    ks = ks < 1 ? 1 : ks;
+    ks = ks > 16 ? 16 : ks;
+    ks = ks > KB ? KB : ks;
+    r.kb_per = (KB + ks - 1) / ks;
+    r.ksplit = (KB + r.kb_per - 1) / r.kb_per;
+  } else {
+    // one block per expert row keeps up to 4 x 256 16-byte vectors in registers
+    r.kc = dtype == MOE_BF16 ? 8192 : 4096;
+    r.ksplit = (d + r.kc - 1) / r.kc;
+  }
+  return r;
+}
+
 WsLayout ws_layout(const moe_layer_desc& D) {
   WsLayout L{};
   const size_t T = (size_t)D.T, E = (size_t)D.E, k = (size_t)D.k, S = (size_t)D.S;
@@ -164,7 +187,7 @@ WsLayout ws_layout(const moe_layer_desc& D) {
     return o;
   };
   L.flags = take(16);
-  L.logits = take(T * E * 4);
+  L.logits = take((size_t)router_plan(D.dtype, D.T, D.d, D.E).ksplit * T * E * 4);
   L.topk_ids = take(T * k * 4);
   L.topk_w = take(T * k * 4);
   L.offsets = take((nE + 1) * 4);

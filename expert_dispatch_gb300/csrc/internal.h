@@ -13,7 +13,7 @@ namespace moe {
 // layer record; P = T * (k + S) is the number of (token, slot) pairs.
 struct WsLayout {
   size_t flags;        // int32[4]: [0] error bits, [1] plan ticket
-  size_t logits;       // fp32 [T, E]
+  size_t logits;       // fp32 [ksplit, T, E] partial router logits
   size_t topk_ids;     // int32 [T, k]
   size_t topk_w;       // fp32 [T, k]
   size_t offsets;      // int32 [E+S+1]
@@ -51,14 +51,26 @@ void count_launch();
 // ---------------------------------------------------------------- launchers
 // Each returns cudaSuccess or the launch error.
 
-// logits[T, E] = x[T, d] * Wr[E, d]^T (+ logit_bias), fp32 accumulate, CUDA cores.
-cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, int T, int d,
-                                      int E, float* logits, cudaStream_t s);
-// tcgen05 version (bf16); returns cudaErrorNotSupported when the shape does not fit.
+// Router logits are produced as ksplit partial sums over K chunks,
+// partial[chunk][T][E] fp32, summed in chunk order by the top-k kernel.
+struct RouterPlan {
+  int tc;      // 1: tcgen05 kernel (bf16, T >= 128, E >= 128); 0: CUDA-core split-K kernel
+  int ksplit;  // number of K chunks (partial logit slices)
+  int kb_per;  // tcgen05: 64-wide K blocks per chunk
+  int kc;      // CUDA cores: elements per chunk
+};
+RouterPlan router_plan(int dtype, int T, int d, int E);
+
+// CUDA cores: one warp per (expert, K chunk), router weights read once.
+cudaError_t launch_router_logits_splitk(int dtype, const void* x, const void* Wr, int T, int d,
+                                        int E, int kc, int ksplit, float* partial,
+                                        cudaStream_t s);
+// tcgen05 (bf16): 128 experts x 128 tokens x K chunk per unit.
 cudaError_t launch_router_logits_tc(const void* x, const void* Wr, int T, int d, int E,
-                                    float* logits, int* err, cudaStream_t s);
-// per-token top-k and gate weights from logits
-cudaError_t launch_router_topk(const float* logits, const float* logit_bias,
+                                    int ksplit, int kb_per, float* partial, int* err,
+                                    cudaStream_t s);
+// per-token top-k and gate weights from the partial logits
+cudaError_t launch_router_topk(const float* partial, int ksplit, const float* logit_bias,
                                const float* sel_bias, int T, int E, int k, int gate,
                                int norm_topk, float rs, int32_t* ids, float* w, cudaStream_t s);
 

@@ -145,6 +145,115 @@ __global__ void plan_place(const int32_t* __restrict__ ids, const float* __restr
   if (slot_w) slot_w[pos] = (j < k && topk_w) ? topk_w[(size_t)t * k + j] : 1.f;
 }
 
+// Block-wide exclusive scan for any blockDim.x that is a multiple of 32.
+__device__ int block_exclusive_scan_any(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int s = lane < nwarps ? warp_sums[lane] : 0;
+    int si = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, si, o);
+      if (lane >= o) si += u;
+    }
+    if (lane < nwarps) warp_sums[lane] = si - s;
+    if (lane == 31) *total = si;
+  }
+  __syncthreads();
+  const int r = warp_sums[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+// The whole plan in one block, for problems whose token bitmaps fit in
+// shared memory: the three steps above with the bitmaps, word prefixes and
+// offsets kept on chip.  Same results, one launch.
+constexpr int kSmallPlanThreads = 1024;
+constexpr int kSmallPlanMaxWords = 4096;
+
+__global__ void __launch_bounds__(kSmallPlanThreads) plan_small(
+    const int32_t* __restrict__ ids, const float* __restrict__ topk_w, int T, int E, int k,
+    int S, int nw, int32_t* __restrict__ offsets, int32_t* __restrict__ tok_idx,
+    int32_t* __restrict__ slot_row, int32_t* __restrict__ active, int32_t* __restrict__ n_active,
+    float* __restrict__ slot_w, int* __restrict__ flags) {
+  extern __shared__ uint32_t sm[];
+  __shared__ int warp_sums[32];
+  __shared__ int chunk_total;
+  const int nE = E + S, ks = k + S;
+  const int nwords = nE * nw;
+  uint32_t* bits = sm;
+  int* wpre = reinterpret_cast<int*>(sm + nwords);
+  int* off = wpre + nwords;  // nE + 1
+  const int P = T * ks;
+  for (int i = threadIdx.x; i < nwords; i += blockDim.x) bits[i] = 0;
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int t = p / ks, j = p - t * ks;
+    const int e = pair_expert(ids, t, j, k, E);
+    if (j < k && (e < 0 || e >= E)) {
+      flag_error(flags, kErrDeviceInput);
+      continue;
+    }
+    const uint32_t bit = 1u << (t & 31);
+    if (atomicOr(&bits[e * nw + (t >> 5)], bit) & bit) flag_error(flags, kErrDeviceInput);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < nE; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < nw; ++w) {
+      wpre[e * nw + w] = run;
+      run += __popc(bits[e * nw + w]);
+    }
+    off[e] = run;  // batch size for now
+  }
+  __syncthreads();
+  int base = 0, abase = 0;
+  for (int e0 = 0; e0 < nE; e0 += blockDim.x) {
+    const int e = e0 + threadIdx.x;
+    const int c = e < nE ? off[e] : 0;
+    const int ex = block_exclusive_scan_any(c, warp_sums, &chunk_total);
+    if (e < nE) {
+      off[e] = base + ex;
+      offsets[e] = base + ex;
+    }
+    base += chunk_total;
+    __syncthreads();
+    const int a = (e < nE && c > 0) ? 1 : 0;
+    const int aex = block_exclusive_scan_any(a, warp_sums, &chunk_total);
+    if (a && active) active[abase + aex] = e;
+    abase += chunk_total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    off[nE] = base;
+    offsets[nE] = base;
+    if (n_active) *n_active = abase;
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int t = p / ks, j = p - t * ks;
+    const int e = pair_expert(ids, t, j, k, E);
+    if (j < k && (e < 0 || e >= E)) {
+      slot_row[p] = -1;
+      continue;
+    }
+    const int wi = e * nw + (t >> 5);
+    const int pos = off[e] + wpre[wi] + __popc(bits[wi] & ((1u << (t & 31)) - 1u));
+    tok_idx[pos] = t;
+    slot_row[p] = pos;
+    if (slot_w) slot_w[pos] = (j < k && topk_w) ? topk_w[(size_t)t * k + j] : 1.f;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_plan(const int32_t* ids, const float* topk_w, int T, int E, int k, int S,
@@ -154,6 +263,14 @@ cudaError_t launch_plan(const int32_t* ids, const float* topk_w, int T, int E, i
   const int nE = E + S;
   const int nw = (T + 31) / 32;
   const long long P = (long long)T * (k + S);
+  if ((long long)nE * nw <= kSmallPlanMaxWords && P <= 64ll * kSmallPlanThreads) {
+    const size_t smem = sizeof(uint32_t) * (2 * (size_t)nE * nw + nE + 1);
+    ProfScope pr("plan_small", s);
+    count_launch();
+    plan_small<<<1, kSmallPlanThreads, smem, s>>>(ids, topk_w, T, E, k, S, nw, offsets, tok_idx,
+                                                  slot_row, active, n_active, slot_w, flags);
+    return cudaGetLastError();
+  }
   cudaError_t err = cudaMemsetAsync(bits, 0, sizeof(uint32_t) * (size_t)nE * nw, s);
   if (err != cudaSuccess) return err;
   err = cudaMemsetAsync(flags + 1, 0, sizeof(int), s);  // ticket

@@ -48,7 +48,10 @@ __device__ __forceinline__ void add8(float (&acc)[8], uint4 v, float w) {
   }
 }
 
-// One block per token; each thread owns 8 consecutive columns per pass.
+// Block (token t, 1024-column slice): the token's slot rows and weights are
+// staged in shared memory, then each thread owns 8 consecutive columns.
+constexpr int kCombineMaxSlots = 36;  // k <= 32, S <= 4
+
 template <bool BF16>
 __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ y_perm,
                                                       const int32_t* __restrict__ slot_row,
@@ -56,15 +59,24 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ y
                                                       const float* __restrict__ residual, int d,
                                                       int k, int S, int P,
                                                       float* __restrict__ y) {
+  __shared__ int rows_s[kCombineMaxSlots];
+  __shared__ float w_s[kCombineMaxSlots];
   const int t = blockIdx.x;
   const int ks = k + S;
-  const int32_t* sr = slot_row + (size_t)t * ks;
-  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+  if (threadIdx.x < ks) {
+    const int j = threadIdx.x;
+    const int r = slot_row[(size_t)t * ks + j];
+    rows_s[j] = (r < 0 || r >= P) ? -1 : r;  // dropped pair (or a row outside the batch rows)
+    w_s[j] = (j < k && topk_w) ? topk_w[(size_t)t * k + j] : 1.f;
+  }
+  __syncthreads();
+  const int c = blockIdx.y * 1024 + threadIdx.x * 8;
+  if (c < d) {
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < ks; ++j) {
-      const int r = sr[j];
-      if (r < 0 || r >= P) continue;  // dropped pair (or a row outside the batch rows)
-      const float w = (j < k && topk_w) ? topk_w[(size_t)t * k + j] : 1.f;
+      const int r = rows_s[j];
+      if (r < 0) continue;
+      const float w = w_s[j];
       if (BF16) {
         const uint4 v = *reinterpret_cast<const uint4*>(
             static_cast<const __nv_bfloat16*>(y_perm) + (size_t)r * d + c);
@@ -117,10 +129,11 @@ cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_ro
   const int P = T * (k + S);
   ProfScope pr("combine", s);
   count_launch();
+  const dim3 grid(T, (d + 1023) / 1024);
   if (dtype == MOE_BF16)
-    combine_kernel<true><<<T, 128, 0, s>>>(y_perm, slot_row, topk_w, residual, d, k, S, P, y);
+    combine_kernel<true><<<grid, 128, 0, s>>>(y_perm, slot_row, topk_w, residual, d, k, S, P, y);
   else
-    combine_kernel<false><<<T, 128, 0, s>>>(y_perm, slot_row, topk_w, residual, d, k, S, P, y);
+    combine_kernel<false><<<grid, 128, 0, s>>>(y_perm, slot_row, topk_w, residual, d, k, S, P, y);
   return cudaGetLastError();
 }
 

@@ -137,29 +137,130 @@ __global__ void __launch_bounds__(256) simt_grouped_gemm_nt(
   }
 }
 
-// One warp per token.  Selection score: logit (softmax family) or
-// sigmoid(logit) + sel_bias (sigmoid family), where logit includes the
-// optional per-expert logit bias.  k rounds of a warp arg-max pick the
-// experts in descending score (ties and NaNs resolved toward the lower index).
-constexpr int kTopkMaxPerLane = 32;  // E <= 1024
+// Router logits for small batches, split over K.  One warp per expert row,
+// 8 experts per block, blockIdx.y = K chunk of kc elements: the warp keeps its
+// chunk of Wr[e] in registers and dots it with every token's chunk of x, so
+// the router weights are read exactly once; partial[chunk][t][e] is summed in
+// chunk order by the top-k kernel (deterministic).  kc is a multiple of 32
+// 16-byte vectors' worth of elements (kc <= 4 * 32 * vector width).
+template <typename T>
+__device__ __forceinline__ float dot16(const uint4& a, const uint4& b);
+template <>
+__device__ __forceinline__ float dot16<__nv_bfloat16>(const uint4& a, const uint4& b) {
+  const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+  const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
+    s = fmaf(fa.x, fb.x, s);
+    s = fmaf(fa.y, fb.y, s);
+  }
+  return s;
+}
+template <>
+__device__ __forceinline__ float dot16<float>(const uint4& a, const uint4& b) {
+  float s = __uint_as_float(a.x) * __uint_as_float(b.x);
+  s = fmaf(__uint_as_float(a.y), __uint_as_float(b.y), s);
+  s = fmaf(__uint_as_float(a.z), __uint_as_float(b.z), s);
+  return fmaf(__uint_as_float(a.w), __uint_as_float(b.w), s);
+}
 
+// Router logits for small batches on CUDA cores.  One block per expert row
+// (blockIdx.x = e; blockIdx.y = K chunk when d is larger than one block keeps
+// in registers): the 8 warps split the chunk's 16-byte vectors, keep their
+// share of Wr[e] in registers, and dot it with every token's x; the 8 warp
+// sums are then added in warp order, so each logit slice is bit-reproducible.
+// Router weights are read exactly once.
+constexpr int kSplitMaxVecPerLane = 4;
+constexpr int kSplitTokChunk = 32;
+
+template <typename T>
+__global__ void __launch_bounds__(256) router_logits_splitk(const T* __restrict__ x,
+                                                            const T* __restrict__ Wr, int ntok,
+                                                            int d, int E, int kc,
+                                                            float* __restrict__ partial) {
+  constexpr int VEC = 16 / sizeof(T);
+  __shared__ float wsum[8][kSplitTokChunk];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x;
+  const int chunk = blockIdx.y;
+  const int k0 = chunk * kc;
+  const int nvec = (min(d, k0 + kc) - k0) / VEC;
+  const uint4* wrow = reinterpret_cast<const uint4*>(Wr + (size_t)e * d + k0);
+  uint4 w[kSplitMaxVecPerLane];
+#pragma unroll
+  for (int i = 0; i < kSplitMaxVecPerLane; ++i) {
+    const int v = warp * 32 + lane + 256 * i;
+    w[i] = v < nvec ? __ldg(wrow + v) : make_uint4(0, 0, 0, 0);
+  }
+  for (int tc = 0; tc < ntok; tc += kSplitTokChunk) {
+    const int nt = min(kSplitTokChunk, ntok - tc);
+    for (int tl = 0; tl < nt; ++tl) {
+      const uint4* xrow = reinterpret_cast<const uint4*>(x + (size_t)(tc + tl) * d + k0);
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < kSplitMaxVecPerLane; ++i) {
+        const int v = warp * 32 + lane + 256 * i;
+        if (v < nvec) acc += dot16<T>(w[i], __ldg(xrow + v));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) wsum[warp][tl] = acc;
+    }
+    __syncthreads();
+    if (threadIdx.x < nt) {
+      float s = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) s += wsum[q][threadIdx.x];
+      partial[((size_t)chunk * ntok + tc + threadIdx.x) * E + e] = s;
+    }
+    __syncthreads();
+  }
+}
+
+// tpb (1 or 8) tokens per block.  First the whole block forms the logits in shared
+// memory: logit = (sum over K chunks of the partial logits, in chunk order)
+// + the optional per-expert logit bias.  Then one warp per token: selection
+// score = logit (softmax family) or sigmoid(logit) + sel_bias (sigmoid
+// family); k rounds of a warp arg-max pick the experts in descending score
+// (ties and NaNs resolved toward the lower index).  Each lane caches the best
+// of its own PL experts, so a round is one warp arg-max plus a rescan by the
+// lane that lost its best.
+constexpr int kTopkTokens = 8;
+constexpr int kTopkMaxExperts = 1024;
+
+template <int PL>  // experts per lane: E <= 32 * PL
 __global__ void __launch_bounds__(256) router_topk_kernel(
-    const float* __restrict__ logits, const float* __restrict__ logit_bias,
-    const float* __restrict__ sel_bias, int T, int E, int k, int gate, int norm_topk, float rs,
-    int32_t* __restrict__ ids, float* __restrict__ w) {
+    const float* __restrict__ partial, int ksplit, const float* __restrict__ logit_bias,
+    const float* __restrict__ sel_bias, int T, int tpb, int E, int k, int gate, int norm_topk,
+    float rs, int32_t* __restrict__ ids, float* __restrict__ w) {
+  __shared__ float lg_s[kTopkTokens][32 * PL];
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const float* lt = logits + (size_t)t * E;
-  float lg[kTopkMaxPerLane], sc[kTopkMaxPerLane];
+  const int t0 = blockIdx.x * tpb;
+  const int ntok = min(tpb, T - t0);
+  for (int idx = threadIdx.x; idx < ntok * E; idx += blockDim.x) {
+    const int tl = idx / E, e = idx - tl * E;
+    const float* src = partial + (size_t)(t0 + tl) * E + e;
+    float l = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < ksplit; ++c) l += src[(size_t)c * T * E];
+    lg_s[tl][e] = l + (logit_bias ? logit_bias[e] : 0.f);
+  }
+  __syncthreads();
+  const int tl = threadIdx.x >> 5;
+  const int t = t0 + tl;
+  if (tl >= ntok) return;
+  float lg[PL], sc[PL];
   uint32_t taken = 0;
 #pragma unroll
-  for (int i = 0; i < kTopkMaxPerLane; ++i) {
+  for (int i = 0; i < PL; ++i) {
     const int e = lane + 32 * i;
     float l = -INFINITY, s = -INFINITY;
     if (e < E) {
-      l = lt[e] + (logit_bias ? logit_bias[e] : 0.f);
-      s = gate == MOE_GATE_SOFTMAX_TOPK ? l : 1.f / (1.f + expf(-l)) + (sel_bias ? sel_bias[e] : 0.f);
+      l = lg_s[tl][e];
+      s = gate == MOE_GATE_SOFTMAX_TOPK ? l
+                                        : 1.f / (1.f + expf(-l)) + (sel_bias ? sel_bias[e] : 0.f);
       if (s != s) s = -INFINITY;
     } else {
       taken |= 1u << i;  // not an expert
@@ -167,33 +268,42 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     lg[i] = l;
     sc[i] = s;
   }
-  int my_id = 0;
-  float my_w = 0.f;
   // softmax normaliser over all experts
   float m = -INFINITY, z = 0.f;
   if (gate == MOE_GATE_SOFTMAX_TOPK) {
 #pragma unroll
-    for (int i = 0; i < kTopkMaxPerLane; ++i) m = fmaxf(m, lg[i]);
+    for (int i = 0; i < PL; ++i) m = fmaxf(m, lg[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
 #pragma unroll
-    for (int i = 0; i < kTopkMaxPerLane; ++i)
+    for (int i = 0; i < PL; ++i)
       if (lane + 32 * i < E) z += expf(lg[i] - m);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
   }
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY, bl = 0.f;
-    int be = 0x7fffffff;
+  // best untaken expert of this lane
+  float lbv = -INFINITY, lbl = 0.f;
+  int lbe = 0x7fffffff;
+  auto rescan = [&]() {
+    lbv = -INFINITY;
+    lbe = 0x7fffffff;
+    lbl = 0.f;
 #pragma unroll
-    for (int i = 0; i < kTopkMaxPerLane; ++i) {
+    for (int i = 0; i < PL; ++i) {
       const int e = lane + 32 * i;
-      if (!(taken & (1u << i)) && (sc[i] > bv || (sc[i] == bv && e < be))) {
-        bv = sc[i];
-        be = e;
-        bl = lg[i];
+      if (!((taken >> i) & 1u) && (sc[i] > lbv || (sc[i] == lbv && e < lbe))) {
+        lbv = sc[i];
+        lbe = e;
+        lbl = lg[i];
       }
     }
+  };
+  rescan();
+  int my_id = 0;
+  float my_w = 0.f;
+  for (int j = 0; j < k; ++j) {
+    float bv = lbv, bl = lbl;
+    int be = lbe;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -205,7 +315,10 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
         bl = ol;
       }
     }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);  // the owning lane retires it
+    if ((be & 31) == lane) {  // the owning lane retires it and finds its next best
+      taken |= 1u << (be >> 5);
+      rescan();
+    }
     const float wj = gate == MOE_GATE_SOFTMAX_TOPK ? expf(bl - m) / z : 1.f / (1.f + expf(-bl));
     if (lane == j) {
       my_id = be;
@@ -213,7 +326,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     }
   }
   if (norm_topk) {
-    float s = lane < k ? my_w : 0.f;
+    const float s = lane < k ? my_w : 0.f;
     // fixed-order sum over the selected slots (slot 0 first)
     float tot = 0.f;
     for (int j = 0; j < k; ++j) tot += __shfl_sync(0xffffffffu, s, j);
@@ -227,31 +340,50 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
 
 }  // namespace
 
-cudaError_t launch_router_logits_simt(int dtype, const void* x, const void* Wr, int T, int d,
-                                      int E, float* logits, cudaStream_t s) {
+cudaError_t launch_router_logits_splitk(int dtype, const void* x, const void* Wr, int T, int d,
+                                        int E, int kc, int ksplit, float* partial,
+                                        cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  dim3 grid((E + kBN - 1) / kBN, (T + kBM - 1) / kBM), block(256);
-  ProfScope p("router_logits_simt", s);
+  const int vec = dtype == MOE_BF16 ? 8 : 4;
+  if (kc % vec || kc > kSplitMaxVecPerLane * 256 * vec || (long long)kc * ksplit < d)
+    return cudaErrorInvalidValue;
+  dim3 grid(E, ksplit), block(256);
+  ProfScope p("router_logits_splitk", s);
   count_launch();
   if (dtype == MOE_BF16)
-    simt_grouped_gemm_nt<__nv_bfloat16, false><<<grid, block, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), nullptr, 1, T,
-        static_cast<const __nv_bfloat16*>(Wr), nullptr, 0, E, d, logits, E, nullptr);
+    router_logits_splitk<__nv_bfloat16><<<grid, block, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(Wr), T, d, E, kc,
+        partial);
   else
-    simt_grouped_gemm_nt<float, false><<<grid, block, 0, s>>>(
-        static_cast<const float*>(x), nullptr, 1, T, static_cast<const float*>(Wr), nullptr, 0,
-        E, d, logits, E, nullptr);
+    router_logits_splitk<float><<<grid, block, 0, s>>>(static_cast<const float*>(x),
+                                                       static_cast<const float*>(Wr), T, d, E,
+                                                       kc, partial);
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_topk(const float* logits, const float* logit_bias,
+cudaError_t launch_router_topk(const float* partial, int ksplit, const float* logit_bias,
                                const float* sel_bias, int T, int E, int k, int gate,
                                int norm_topk, float rs, int32_t* ids, float* w, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   ProfScope p("router_topk", s);
   count_launch();
-  router_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, logit_bias, sel_bias, T, E, k, gate,
-                                                 norm_topk, rs, ids, w);
+  // small batches: one token per block so that the partial sums spread over many SMs
+  const int tpb = T < 8 * 152 ? 1 : kTopkTokens;
+  const int nb = (T + tpb - 1) / tpb;
+#define MOE_TOPK(PL)                                                                   \
+  router_topk_kernel<PL><<<nb, 256, 0, s>>>(partial, ksplit, logit_bias, sel_bias, T, \
+                                            tpb, E, k, gate, norm_topk, rs, ids, w)
+  if (E <= 128)
+    MOE_TOPK(4);
+  else if (E <= 256)
+    MOE_TOPK(8);
+  else if (E <= 384)
+    MOE_TOPK(12);
+  else if (E <= 512)
+    MOE_TOPK(16);
+  else
+    MOE_TOPK(32);
+#undef MOE_TOPK
   return cudaGetLastError();
 }
 

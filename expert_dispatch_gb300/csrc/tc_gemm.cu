@@ -40,7 +40,8 @@ namespace {
 
 constexpr int MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2;
 constexpr int kMaxGroups = 1028;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                   // two per TMEM lane quarter
+constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, epilogue
 
 template <int MODE, int BN, int STAGES>
 struct Cfg {
@@ -75,15 +76,21 @@ struct Params {
   const float* row_scale;  // MODE_DOWN: per-row factor or null
   int* err;
   int max_rows;            // rows of the token operand / output; batch bounds are clamped to it
+  int ksplit;              // MODE_ROUTER: K is cut into ksplit chunks of kb_per 64-wide blocks,
+  int kb_per;              //   each chunk's partial sums go to out + chunk * rows * ldo
 };
 
 struct Unit {
-  int g, mt, r0, nt;
+  int g, mt, r0, nt, kb0, kb1;
 };
 
-template <int BN>
+// Unit u -> (group, weight block, token rows, K range).  Units of a group are
+// ordered weight-block-minor: the CTAs running at the same time cover all
+// weight blocks of a few token tiles, so an expert's weights and those token
+// rows stay in L2 while its token tiles are swept.
+template <int MODE, int BN>
 __device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int* gstart,
-                                            int n_groups, int m_tiles) {
+                                            int n_groups, int m_tiles, int KB, const Params& p) {
   int lo = 0, hi = n_groups - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -92,14 +99,23 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int*
   const int local = u - prefix[lo];
   const int cnt = gstart[lo + 1] - gstart[lo];
   const int tiles = (cnt + BN - 1) / BN;
-  const int mt = local / tiles;
-  const int tt = local - mt * tiles;
+  int mt, tt, ks = 0;
+  if (MODE == MODE_ROUTER) {
+    mt = local % m_tiles;
+    const int rest = local / m_tiles;
+    tt = rest % tiles;
+    ks = rest / tiles;
+  } else {
+    mt = local % m_tiles;
+    tt = local / m_tiles;
+  }
   Unit r;
   r.g = lo;
   r.mt = mt;
   r.r0 = gstart[lo] + tt * BN;
   r.nt = min(BN, cnt - tt * BN);
-  (void)m_tiles;
+  r.kb0 = MODE == MODE_ROUTER ? ks * p.kb_per : 0;
+  r.kb1 = MODE == MODE_ROUTER ? min(KB, r.kb0 + p.kb_per) : KB;
   return r;
 }
 
@@ -141,7 +157,8 @@ template <int MODE, int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
-                    const __grid_constant__ CUtensorMap tmB, const Params p) {
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmBfull, const Params p) {
   using C = Cfg<MODE, BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -169,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < C::NBUF; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 4);
+      mbar_init(acce_bar(b), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -177,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA0);
     if (C::NA == 2) tma_prefetch_desc(&tmA1);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmBfull);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -212,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int units = 0;
       if (g < p.n_groups) {
         const int cnt = gstart[g + 1] - gstart[g];
-        units = m_tiles * ((cnt + BN - 1) / BN);
+        units = m_tiles * ((cnt + BN - 1) / BN) * (MODE == MODE_ROUTER ? p.ksplit : 1);
       }
       int incl = units;
 #pragma unroll
@@ -236,12 +254,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x) {
-        const Unit t = decode_unit<BN>(u, prefix, gstart, p.n_groups, m_tiles);
+        const Unit t = decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
         const int nchunks = (t.nt + 31) / 32;
         const uint32_t bytes = C::NA * C::A_BYTES + nchunks * 4096;
         const int arow = t.g * p.Mg + t.mt * 128;
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
@@ -253,8 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sA, &tmA0, full_bar(stage), kb * 64, arow);
           if (C::NA == 2) tma_load_2d(sA + C::A_BYTES, &tmA1, full_bar(stage), kb * 64, arow);
           const uint32_t sB = sA + C::NA * C::A_BYTES;
-          for (int c = 0; c < nchunks; ++c)
-            tma_load_2d(sB + c * 4096, &tmB, full_bar(stage), kb * 64, t.r0 + c * 32);
+          if (t.nt == BN)  // a full token tile: one box of BN rows
+            tma_load_2d(sB, &tmBfull, full_bar(stage), kb * 64, t.r0);
+          else
+            for (int c = 0; c < nchunks; ++c)
+              tma_load_2d(sB + c * 4096, &tmB, full_bar(stage), kb * 64, t.r0 + c * 32);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -273,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool issued = false;
       for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x, ++it) {
-        const Unit t = decode_unit<BN>(u, prefix, gstart, p.n_groups, m_tiles);
+        const Unit t = decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
         const int n_mma = max(16, (t.nt + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(128, n_mma);
         const int buf = C::NBUF == 2 ? (it & 1) : 0;
@@ -282,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d0 = tmem_base + (uint32_t)(buf * C::NACC * BN);
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!mbar_wait(full_bar(stage), phase, abort_flag, p.err)) {
             ok = false;
             break;
@@ -293,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bdesc = smem_desc_sw128(sB + kk * 32);
-            const uint32_t acc = (kb | kk) != 0;
+            const uint32_t acc = (kb != t.kb0 || kk != 0) ? 1u : 0u;
             umma_bf16(d0, smem_desc_sw128(sA + kk * 32), bdesc, idesc, acc);
             if (C::NA == 2)
               umma_bf16(d0 + BN, smem_desc_sw128(sA + C::A_BYTES + kk * 32), bdesc, idesc, acc);
@@ -315,11 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // ------------------------------------------------------------ epilogue (warps 2..9)
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int half = (warp - 2) / 4;  // the two warps of a quarter take alternate 16-column chunks
     int it = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-      const Unit t = decode_unit<BN>(u, prefix, gstart, p.n_groups, m_tiles);
+      const Unit t = decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
       const int buf = C::NBUF == 2 ? (it & 1) : 0;
       const uint32_t use = C::NBUF == 2 ? (uint32_t)(it >> 1) : (uint32_t)it;
       if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, p.err)) break;
@@ -327,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = t.mt * 128 + q * 32 + lane;  // weight row within the group
       const bool mvalid = m < p.Mg;
       const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::NACC * BN);
-      for (int c0 = 0; c0 < t.nt; c0 += 16) {
+      for (int c0 = 16 * half; c0 < t.nt; c0 += 32) {
         uint32_t a[16], b[16];
         tmem_ld16(tb + c0, a);
         if (C::NA == 2) tmem_ld16(tb + BN + c0, b);
@@ -340,7 +362,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const size_t row = (size_t)(t.r0 + col);
             const float v = __uint_as_float(a[j]);
             if (MODE == MODE_ROUTER) {
-              static_cast<float*>(p.out)[row * p.ldo + m] = v;
+              const size_t chunk = (size_t)(t.kb0 / p.kb_per);
+              static_cast<float*>(p.out)[(chunk * p.rows_single + row) * p.ldo + m] = v;
             } else if (MODE == MODE_GATEUP) {
               const float hval = silu_f32(v) * __uint_as_float(b[j]);
               static_cast<__nv_bfloat16*>(p.out)[row * p.ldo + m] = __float2bfloat16_rn(hval);
@@ -402,7 +425,8 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
 
 template <int MODE, int BN, int STAGES>
 cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                      const Params& p, long long max_units, const char* name, cudaStream_t s) {
+                      const CUtensorMap& bfull, const Params& p, long long max_units,
+                      const char* name, cudaStream_t s) {
   using C = Cfg<MODE, BN, STAGES>;
   auto kern = tc_grouped_gemm<MODE, BN, STAGES>;
   int dev = 0;
@@ -418,7 +442,7 @@ cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtens
   if (grid <= 0) return cudaSuccess;
   ProfScope pr(name, s);
   count_launch();
-  kern<<<(unsigned)grid, kThreads, C::SMEM_TOTAL, s>>>(a0, a1, b, p);
+  kern<<<(unsigned)grid, kThreads, C::SMEM_TOTAL, s>>>(a0, a1, b, bfull, p);
   return cudaGetLastError();
 }
 
@@ -434,34 +458,40 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
                           cudaStream_t s) {
   if (P == 0) return cudaSuccess;
   const uint64_t cap = (uint64_t)tc_row_capacity(P);
-  CUtensorMap tg, tu, tx, td, th;
+  // token operands: 32-row boxes for partial tiles, 256-row boxes for full ones
+  CUtensorMap tg, tu, tx, tx256, td, th, th256;
   if (!make_tmap(&tg, Wg, d, (uint64_t)n_groups * I, 128) ||
       !make_tmap(&tu, Wu, d, (uint64_t)n_groups * I, 128) ||
-      !make_tmap(&tx, x_perm, d, cap, 32) ||
-      !make_tmap(&td, Wd, I, (uint64_t)n_groups * d, 128) || !make_tmap(&th, h, I, cap, 32))
+      !make_tmap(&tx, x_perm, d, cap, 32) || !make_tmap(&tx256, x_perm, d, cap, 256) ||
+      !make_tmap(&td, Wd, I, (uint64_t)n_groups * d, 128) || !make_tmap(&th, h, I, cap, 32) ||
+      !make_tmap(&th256, h, I, cap, 256))
     return cudaErrorInvalidValue;
   const bool small = mean_rows <= 48.0;
   const int bn = small ? 32 : 256;
   Params p1{offsets, n_groups, 0, I, d, h, I, nullptr, err, P};
   const long long u1 = (long long)((I + 127) / 128) * ((P + bn - 1) / bn + n_groups);
-  cudaError_t e = small ? launch_tc<MODE_GATEUP, 32, 6>(tg, tu, tx, p1, u1, "ffn_gateup_tc", s)
-                        : launch_tc<MODE_GATEUP, 256, 3>(tg, tu, tx, p1, u1, "ffn_gateup_tc", s);
+  cudaError_t e =
+      small ? launch_tc<MODE_GATEUP, 32, 6>(tg, tu, tx, tx, p1, u1, "ffn_gateup_tc", s)
+            : launch_tc<MODE_GATEUP, 256, 3>(tg, tu, tx, tx256, p1, u1, "ffn_gateup_tc", s);
   if (e != cudaSuccess) return e;
   Params p2{offsets, n_groups, 0, d, I, y_perm, d, slot_w, err, P};
   const long long u2 = (long long)((d + 127) / 128) * ((P + bn - 1) / bn + n_groups);
-  return small ? launch_tc<MODE_DOWN, 32, 10>(td, td, th, p2, u2, "ffn_down_tc", s)
-               : launch_tc<MODE_DOWN, 256, 4>(td, td, th, p2, u2, "ffn_down_tc", s);
+  return small ? launch_tc<MODE_DOWN, 32, 10>(td, td, th, th, p2, u2, "ffn_down_tc", s)
+               : launch_tc<MODE_DOWN, 256, 4>(td, td, th, th256, p2, u2, "ffn_down_tc", s);
 }
 
 cudaError_t launch_router_logits_tc(const void* x, const void* Wr, int T, int d, int E,
-                                    float* logits, int* err, cudaStream_t s) {
-  if (T < 256 || E < 128) return cudaErrorNotSupported;
-  CUtensorMap ta, tb;
-  if (!make_tmap(&ta, Wr, d, E, 128) || !make_tmap(&tb, x, d, T, 32))
+                                    int ksplit, int kb_per, float* partial, int* err,
+                                    cudaStream_t s) {
+  if (T < 32 || E < 128 || ksplit < 1 || kb_per < 1) return cudaErrorInvalidValue;
+  // a full 128-token box only exists when T >= 128; below that every unit is partial
+  CUtensorMap ta, tb, tb128;
+  if (!make_tmap(&ta, Wr, d, E, 128) || !make_tmap(&tb, x, d, T, 32) ||
+      !make_tmap(&tb128, x, d, T, T >= 128 ? 128 : 32))
     return cudaErrorInvalidValue;
-  Params p{nullptr, 1, T, E, d, logits, E, nullptr, err, T};
-  const long long units = (long long)((E + 127) / 128) * ((T + 255) / 256);
-  return launch_tc<MODE_ROUTER, 256, 4>(ta, ta, tb, p, units, "router_logits_tc", s);
+  Params p{nullptr, 1, T, E, d, partial, E, nullptr, err, T, ksplit, kb_per};
+  const long long units = (long long)((E + 127) / 128) * ((T + 127) / 128) * ksplit;
+  return launch_tc<MODE_ROUTER, 128, 6>(ta, ta, tb, tb128, p, units, "router_logits_tc", s);
 }
 
 }  // namespace moe

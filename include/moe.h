@@ -213,7 +213,7 @@ int64_t moe_launch_count(void);
    earlier records; moe_profile_enable(0) stops.  moe_profile_query()
    synchronizes on the recorded events and returns, for the named kernel, the
    number of recorded launches and their summed device time in milliseconds.
-   Kernel names: router_logits_simt, router_logits_tc, router_topk,
+   Kernel names: router_logits_splitk, router_logits_tc, router_topk,
    plan_mark, plan_scan, plan_place, gather_rows, ffn_gateup_simt,
    ffn_down_simt, ffn_gateup_tc, ffn_down_tc, combine.                      */
 moe_status moe_profile_enable(int on);
