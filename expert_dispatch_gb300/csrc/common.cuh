@@ -38,6 +38,19 @@ __device__ __forceinline__ float load_as_f32(const __nv_bfloat16* p, size_t i) {
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched so that it may start while its
+// predecessor on the stream is finishing.  The contract that keeps this safe:
+//   * pdl_wait() blocks until the predecessor grid has completed and its
+//     writes are visible; nothing the predecessor writes is touched before it;
+//   * a kernel calls pdl_trigger() only after its own pdl_wait(), so when a
+//     kernel starts, every grid two or more launches back has completed.
+// Both are no-ops for a launch without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- shared-memory addresses
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -26,6 +26,8 @@ __device__ __forceinline__ int pair_expert(const int32_t* ids, int t, int j, int
 
 __global__ void plan_mark(const int32_t* __restrict__ ids, int T, int E, int k, int S,
                           uint32_t* __restrict__ bits, int nw, int* __restrict__ flags) {
+  pdl_wait();     // the predecessor grid is complete and visible
+  pdl_trigger();  // dependents may launch (they wait for this grid in turn)
   const long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int ks = k + S;
   if (p >= (long long)T * ks) return;
@@ -78,6 +80,8 @@ __global__ void __launch_bounds__(256) plan_scan(const uint32_t* __restrict__ bi
                                                  int32_t* __restrict__ active,
                                                  int32_t* __restrict__ n_active,
                                                  int* __restrict__ ticket) {
+  pdl_wait();     // the predecessor grid is complete and visible
+  pdl_trigger();  // dependents may launch (they wait for this grid in turn)
   __shared__ int warp_sums[8];
   __shared__ int chunk_total;
   __shared__ int is_last;
@@ -128,6 +132,8 @@ __global__ void plan_place(const int32_t* __restrict__ ids, const float* __restr
                            const int32_t* __restrict__ wpre, const int32_t* __restrict__ offsets,
                            int32_t* __restrict__ tok_idx, int32_t* __restrict__ slot_row,
                            float* __restrict__ slot_w) {
+  pdl_wait();     // the predecessor grid is complete and visible
+  pdl_trigger();  // dependents may launch (they wait for this grid in turn)
   const long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int ks = k + S;
   if (p >= (long long)T * ks) return;
@@ -185,6 +191,8 @@ __global__ void __launch_bounds__(kSmallPlanThreads) plan_small(
     int S, int nw, int32_t* __restrict__ offsets, int32_t* __restrict__ tok_idx,
     int32_t* __restrict__ slot_row, int32_t* __restrict__ active, int32_t* __restrict__ n_active,
     float* __restrict__ slot_w, int* __restrict__ flags) {
+  pdl_wait();     // the predecessor grid is complete and visible
+  pdl_trigger();  // dependents may launch (they wait for this grid in turn)
   extern __shared__ uint32_t sm[];
   __shared__ int warp_sums[32];
   __shared__ int chunk_total;
@@ -266,8 +274,7 @@ cudaError_t launch_plan(const int32_t* ids, const float* topk_w, int T, int E, i
   if ((long long)nE * nw <= kSmallPlanMaxWords && P <= 64ll * kSmallPlanThreads) {
     const size_t smem = sizeof(uint32_t) * (2 * (size_t)nE * nw + nE + 1);
     ProfScope pr("plan_small", s);
-    count_launch();
-    plan_small<<<1, kSmallPlanThreads, smem, s>>>(ids, topk_w, T, E, k, S, nw, offsets, tok_idx,
+    (void)launch_kernel(plan_small, 1, kSmallPlanThreads, smem, s, ids, topk_w, T, E, k, S, nw, offsets, tok_idx,
                                                   slot_row, active, n_active, slot_w, flags);
     return cudaGetLastError();
   }
@@ -278,21 +285,18 @@ cudaError_t launch_plan(const int32_t* ids, const float* topk_w, int T, int E, i
   const int nb = (int)((P + 255) / 256);
   {
     ProfScope pr("plan_mark", s);
-    count_launch();
-    plan_mark<<<nb, 256, 0, s>>>(ids, T, E, k, S, bits, nw, flags);
+    (void)launch_kernel(plan_mark, nb, 256, 0, s, ids, T, E, k, S, bits, nw, flags);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   {
     ProfScope pr("plan_scan", s);
-    count_launch();
-    plan_scan<<<nE, 256, 0, s>>>(bits, nw, nE, wpre, counts, offsets, active, n_active,
+    (void)launch_kernel(plan_scan, nE, 256, 0, s, bits, nw, nE, wpre, counts, offsets, active, n_active,
                                  flags + 1);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
   }
   {
     ProfScope pr("plan_place", s);
-    count_launch();
-    plan_place<<<nb, 256, 0, s>>>(ids, topk_w, T, E, k, S, bits, nw, wpre, offsets, tok_idx,
+    (void)launch_kernel(plan_place, nb, 256, 0, s, ids, topk_w, T, E, k, S, bits, nw, wpre, offsets, tok_idx,
                                   slot_row, slot_w);
   }
   return cudaGetLastError();

@@ -25,6 +25,8 @@ namespace {
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ tok,
                                    const int32_t* __restrict__ total_rows, int P, int T,
                                    int vec_per_row, uint4* __restrict__ x_perm, int* flags) {
+  pdl_wait();     // the predecessor grid is complete and visible
+  pdl_trigger();  // dependents may launch (they wait for this grid in turn)
   const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= P || r >= *total_rows) return;
@@ -59,6 +61,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ y
                                                       const float* __restrict__ residual, int d,
                                                       int k, int S, int P,
                                                       float* __restrict__ y) {
+  pdl_wait();     // the predecessor grid is complete and visible
+  pdl_trigger();  // dependents may launch (they wait for this grid in turn)
   __shared__ int rows_s[kCombineMaxSlots];
   __shared__ float w_s[kCombineMaxSlots];
   const int t = blockIdx.x;
@@ -115,8 +119,7 @@ cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* tok_idx,
   if (P == 0) return cudaSuccess;
   const int vec = (int)(d * dtype_size(dtype) / 16);
   ProfScope pr("gather_rows", s);
-  count_launch();
-  gather_rows_kernel<<<(P + 7) / 8, 256, 0, s>>>(static_cast<const uint4*>(x), tok_idx,
+  (void)launch_kernel(gather_rows_kernel, (P + 7) / 8, 256, 0, s, static_cast<const uint4*>(x), tok_idx,
                                                  total_rows, P, T, vec,
                                                  static_cast<uint4*>(x_perm), flags);
   return cudaGetLastError();
@@ -128,12 +131,11 @@ cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_ro
   if (T == 0) return cudaSuccess;
   const int P = T * (k + S);
   ProfScope pr("combine", s);
-  count_launch();
   const dim3 grid(T, (d + 1023) / 1024);
   if (dtype == MOE_BF16)
-    combine_kernel<true><<<grid, 128, 0, s>>>(y_perm, slot_row, topk_w, residual, d, k, S, P, y);
+    (void)launch_kernel(combine_kernel<true>, grid, 128, 0, s, y_perm, slot_row, topk_w, residual, d, k, S, P, y);
   else
-    combine_kernel<false><<<grid, 128, 0, s>>>(y_perm, slot_row, topk_w, residual, d, k, S, P, y);
+    (void)launch_kernel(combine_kernel<false>, grid, 128, 0, s, y_perm, slot_row, topk_w, residual, d, k, S, P, y);
   return cudaGetLastError();
 }
 

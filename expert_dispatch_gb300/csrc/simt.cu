@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(256) simt_grouped_gemm_nt(
     const T* __restrict__ A, const int32_t* __restrict__ offsets, int n_groups, int rows_single,
     const T* __restrict__ B0, const T* __restrict__ B1, long long b_group_stride, int N, int K,
     float* __restrict__ C, int ldc, const float* __restrict__ row_scale) {
+  pdl_wait();     // the predecessor grid is complete and visible
+  pdl_trigger();  // dependents may launch (they wait for this grid in turn)
   __shared__ float As[kBK][kBM + 4];
   __shared__ float Bs0[kBK][kBN + 4];
   __shared__ float Bs1[DUAL ? kBK : 1][kBN + 4];
@@ -180,6 +182,8 @@ __global__ void __launch_bounds__(256) router_logits_splitk(const T* __restrict_
                                                             const T* __restrict__ Wr, int ntok,
                                                             int d, int E, int kc,
                                                             float* __restrict__ partial) {
+  pdl_wait();     // the predecessor grid is complete and visible
+  pdl_trigger();  // dependents may launch (they wait for this grid in turn)
   constexpr int VEC = 16 / sizeof(T);
   __shared__ float wsum[8][kSplitTokChunk];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -235,6 +239,8 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     const float* __restrict__ partial, int ksplit, const float* __restrict__ logit_bias,
     const float* __restrict__ sel_bias, int T, int tpb, int E, int k, int gate, int norm_topk,
     float rs, int32_t* __restrict__ ids, float* __restrict__ w) {
+  pdl_wait();     // the predecessor grid is complete and visible
+  pdl_trigger();  // dependents may launch (they wait for this grid in turn)
   __shared__ float lg_s[kTopkTokens][32 * PL];
   const int lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * tpb;
@@ -349,13 +355,12 @@ cudaError_t launch_router_logits_splitk(int dtype, const void* x, const void* Wr
     return cudaErrorInvalidValue;
   dim3 grid(E, ksplit), block(256);
   ProfScope p("router_logits_splitk", s);
-  count_launch();
   if (dtype == MOE_BF16)
-    router_logits_splitk<__nv_bfloat16><<<grid, block, 0, s>>>(
+    (void)launch_kernel(router_logits_splitk<__nv_bfloat16>, grid, block, 0, s, 
         static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(Wr), T, d, E, kc,
         partial);
   else
-    router_logits_splitk<float><<<grid, block, 0, s>>>(static_cast<const float*>(x),
+    (void)launch_kernel(router_logits_splitk<float>, grid, block, 0, s, static_cast<const float*>(x),
                                                        static_cast<const float*>(Wr), T, d, E,
                                                        kc, partial);
   return cudaGetLastError();
@@ -366,12 +371,11 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, const float* lo
                                int norm_topk, float rs, int32_t* ids, float* w, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   ProfScope p("router_topk", s);
-  count_launch();
   // small batches: one token per block so that the partial sums spread over many SMs
   const int tpb = T < 8 * 152 ? 1 : kTopkTokens;
   const int nb = (T + tpb - 1) / tpb;
 #define MOE_TOPK(PL)                                                                   \
-  router_topk_kernel<PL><<<nb, 256, 0, s>>>(partial, ksplit, logit_bias, sel_bias, T, \
+  (void)launch_kernel(router_topk_kernel<PL>, nb, 256, 0, s, partial, ksplit, logit_bias, sel_bias, T, \
                                             tpb, E, k, gate, norm_topk, rs, ids, w)
   if (E <= 128)
     MOE_TOPK(4);
@@ -395,18 +399,16 @@ cudaError_t launch_ffn_simt(const float* x_perm, const int32_t* offsets, int n_g
   const int max_tiles = (P + kBM - 1) / kBM + n_groups;
   {
     ProfScope p("ffn_gateup_simt", s);
-    count_launch();
     dim3 grid((I + kBN - 1) / kBN, max_tiles);
-    simt_grouped_gemm_nt<float, true><<<grid, 256, 0, s>>>(
+    (void)launch_kernel(simt_grouped_gemm_nt<float, true>, grid, 256, 0, s, 
         x_perm, offsets, n_groups, P, Wg, Wu, (long long)I * d, I, d, h, I, nullptr);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   {
     ProfScope p("ffn_down_simt", s);
-    count_launch();
     dim3 grid((d + kBN - 1) / kBN, max_tiles);
-    simt_grouped_gemm_nt<float, false><<<grid, 256, 0, s>>>(
+    (void)launch_kernel(simt_grouped_gemm_nt<float, false>, grid, 256, 0, s, 
         h, offsets, n_groups, P, Wd, nullptr, (long long)d * I, d, I, y_perm, d, slot_w);
   }
   return cudaGetLastError();

@@ -84,10 +84,12 @@ struct Unit {
   int g, mt, r0, nt, kb0, kb1;
 };
 
-// Unit u -> (group, weight block, token rows, K range).  Units of a group are
-// ordered weight-block-minor: the CTAs running at the same time cover all
-// weight blocks of a few token tiles, so an expert's weights and those token
-// rows stay in L2 while its token tiles are swept.
+// Unit u -> (group, weight block, token rows, K range).  A group with at most
+// four token tiles is ordered token-tile-minor (a weight block's tiles run
+// back to back, so its bytes come from HBM once); a group with more is
+// ordered weight-block-minor (the CTAs running together cover all weight
+// blocks of a few token tiles, so the expert's weights and those token rows
+// stay in L2 while its tiles are swept).  The router always uses the latter.
 template <int MODE, int BN>
 __device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int* gstart,
                                             int n_groups, int m_tiles, int KB, const Params& p) {
@@ -105,7 +107,10 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int*
     const int rest = local / m_tiles;
     tt = rest % tiles;
     ks = rest / tiles;
-  } else {
+  } else if (tiles <= 4) {  // few token tiles: a weight block's tiles back to back
+    mt = local / tiles;
+    tt = local - mt * tiles;
+  } else {  // many token tiles: all weight blocks of a token tile back to back
     mt = local % m_tiles;
     tt = local / m_tiles;
   }
@@ -253,23 +258,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, armed = 0, armed_parity = 0;
+      // Weights are inputs no kernel of this sequence writes, and the unit
+      // schedule comes from a grid two launches back: the first unit's weight
+      // tiles are requested before waiting for the predecessor grid, whose
+      // output (the token rows) is loaded only after the wait.
+      int n_pre = 0;
+      if ((int)blockIdx.x < total) {
+        const Unit t = decode_unit<MODE, BN>(blockIdx.x, prefix, gstart, p.n_groups, m_tiles, KB, p);
+        const uint32_t bytes = C::NA * C::A_BYTES + ((t.nt + 31) / 32) * 4096;
+        const int arow = t.g * p.Mg + t.mt * 128;
+        n_pre = min(STAGES, t.kb1 - t.kb0);
+        for (int i = 0; i < n_pre; ++i) {  // fresh ring: stages 0..n_pre-1 are free
+          mbar_arrive_expect_tx(full_bar(i), bytes);
+          armed |= 1u << i;
+          const uint32_t sA = sbase + i * C::STAGE_BYTES;
+          tma_load_2d(sA, &tmA0, full_bar(i), (t.kb0 + i) * 64, arow);
+          if (C::NA == 2) tma_load_2d(sA + C::A_BYTES, &tmA1, full_bar(i), (t.kb0 + i) * 64, arow);
+        }
+      }
+      pdl_wait();
+      bool first = true;
       for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x) {
+        if (u + (int)gridDim.x >= total) pdl_trigger();  // this CTA's last unit
         const Unit t = decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
         const int nchunks = (t.nt + 31) / 32;
         const uint32_t bytes = C::NA * C::A_BYTES + nchunks * 4096;
         const int arow = t.g * p.Mg + t.mt * 128;
         bool ok = true;
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
-            ok = false;
-            break;
+          const bool pre = first && kb - t.kb0 < n_pre;  // armed, weights already requested
+          if (!pre) {
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full_bar(stage), bytes);
+            armed |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           }
-          mbar_arrive_expect_tx(full_bar(stage), bytes);
-          armed |= 1u << stage;
-          armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           const uint32_t sA = sbase + stage * C::STAGE_BYTES;
-          tma_load_2d(sA, &tmA0, full_bar(stage), kb * 64, arow);
-          if (C::NA == 2) tma_load_2d(sA + C::A_BYTES, &tmA1, full_bar(stage), kb * 64, arow);
+          if (!pre) {
+            tma_load_2d(sA, &tmA0, full_bar(stage), kb * 64, arow);
+            if (C::NA == 2) tma_load_2d(sA + C::A_BYTES, &tmA1, full_bar(stage), kb * 64, arow);
+          }
           const uint32_t sB = sA + C::NA * C::A_BYTES;
           if (t.nt == BN)  // a full token tile: one box of BN rows
             tma_load_2d(sB, &tmBfull, full_bar(stage), kb * 64, t.r0);
@@ -281,8 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1u;
           }
         }
+        first = false;
         if (!ok) break;
       }
+      if ((int)blockIdx.x >= total) pdl_trigger();
       // wind down: every copy this thread started has landed before exit
       for (int s = 0; s < STAGES; ++s)
         if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_parity >> s) & 1u, p.err);
@@ -441,8 +474,7 @@ cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtens
   const long long grid = max_units < num_sms() ? max_units : num_sms();
   if (grid <= 0) return cudaSuccess;
   ProfScope pr(name, s);
-  count_launch();
-  kern<<<(unsigned)grid, kThreads, C::SMEM_TOTAL, s>>>(a0, a1, b, bfull, p);
+  (void)launch_kernel(kern, (unsigned)grid, kThreads, C::SMEM_TOTAL, s, a0, a1, b, bfull, p);
   return cudaGetLastError();
 }
 
@@ -458,26 +490,36 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
                           cudaStream_t s) {
   if (P == 0) return cudaSuccess;
   const uint64_t cap = (uint64_t)tc_row_capacity(P);
-  // token operands: 32-row boxes for partial tiles, 256-row boxes for full ones
-  CUtensorMap tg, tu, tx, tx256, td, th, th256;
+  // Token tiles by mean batch size: 32 rows for decode-sized batches (deep
+  // pipelines).  Above that, gate/up uses 128 rows while batches are a few
+  // hundred rows (its two accumulators then fit twice in TMEM, so the epilogue
+  // overlaps the next unit's MMAs) and 256 rows for larger batches (tensor
+  // bound: the largest MMA); down uses 256 rows (fewest weight passes).
+  const bool small = mean_rows <= 48.0;
+  const int bn = small ? 32 : mean_rows <= 256.0 ? 128 : 256;
+  // token operands: 32-row boxes for partial tiles, tile-high boxes for full ones
+  CUtensorMap tg, tu, tx, txf, td, th, thf, thf2;
   if (!make_tmap(&tg, Wg, d, (uint64_t)n_groups * I, 128) ||
       !make_tmap(&tu, Wu, d, (uint64_t)n_groups * I, 128) ||
-      !make_tmap(&tx, x_perm, d, cap, 32) || !make_tmap(&tx256, x_perm, d, cap, 256) ||
+      !make_tmap(&tx, x_perm, d, cap, 32) || !make_tmap(&txf, x_perm, d, cap, bn) ||
       !make_tmap(&td, Wd, I, (uint64_t)n_groups * d, 128) || !make_tmap(&th, h, I, cap, 32) ||
-      !make_tmap(&th256, h, I, cap, 256))
+      !make_tmap(&thf, h, I, cap, 32) || !make_tmap(&thf2, h, I, cap, 256))
     return cudaErrorInvalidValue;
-  const bool small = mean_rows <= 48.0;
-  const int bn = small ? 32 : 256;
   Params p1{offsets, n_groups, 0, I, d, h, I, nullptr, err, P};
   const long long u1 = (long long)((I + 127) / 128) * ((P + bn - 1) / bn + n_groups);
-  cudaError_t e =
-      small ? launch_tc<MODE_GATEUP, 32, 6>(tg, tu, tx, tx, p1, u1, "ffn_gateup_tc", s)
-            : launch_tc<MODE_GATEUP, 256, 3>(tg, tu, tx, tx256, p1, u1, "ffn_gateup_tc", s);
+  cudaError_t e;
+  if (small)
+    e = launch_tc<MODE_GATEUP, 32, 6>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
+  else if (bn == 128)
+    e = launch_tc<MODE_GATEUP, 128, 4>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
+  else
+    e = launch_tc<MODE_GATEUP, 256, 3>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
   if (e != cudaSuccess) return e;
+  const int bn2 = small ? 32 : 256;
   Params p2{offsets, n_groups, 0, d, I, y_perm, d, slot_w, err, P};
-  const long long u2 = (long long)((d + 127) / 128) * ((P + bn - 1) / bn + n_groups);
-  return small ? launch_tc<MODE_DOWN, 32, 10>(td, td, th, th, p2, u2, "ffn_down_tc", s)
-               : launch_tc<MODE_DOWN, 256, 4>(td, td, th, th256, p2, u2, "ffn_down_tc", s);
+  const long long u2 = (long long)((d + 127) / 128) * ((P + bn2 - 1) / bn2 + n_groups);
+  if (small) return launch_tc<MODE_DOWN, 32, 10>(td, td, th, thf, p2, u2, "ffn_down_tc", s);
+  return launch_tc<MODE_DOWN, 256, 4>(td, td, th, thf2, p2, u2, "ffn_down_tc", s);
 }
 
 cudaError_t launch_router_logits_tc(const void* x, const void* Wr, int T, int d, int E,

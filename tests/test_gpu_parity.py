@@ -168,6 +168,11 @@ FFN_CASES = [
     LayerConfig("f_bf16_skewed", T=700, d=192, E=12, I=128, k=3, zipf_s=1.2),
     LayerConfig("f_bf16_one_token", T=1, d=512, E=32, I=256, k=4, S=1, gate=1, norm_topk=1,
                 routed_scaling=2.8, sel_bias_range=0.1),
+    # ~100 rows per batch: 128-token tiles, shared batch of 300 rows in 3 tiles
+    LayerConfig("f_bf16_mid_tiles", T=300, d=192, E=8, I=320, k=2, S=1, gate=1, norm_topk=1,
+                routed_scaling=2.5, sel_bias_range=0.1),
+    # a hot expert with more than four 256-token tiles (weight-block-minor order)
+    LayerConfig("f_bf16_hot_expert", T=2000, d=128, E=8, I=128, k=2, zipf_s=1.2),
 ]
 
 
