@@ -175,6 +175,18 @@ def traffic_record(kernel, cfg):
     return None
 
 
+def aggregate_ranks(ms, e2e_ms, tokens_per_step, steps, world, device):
+    """Whole-job figures over ranks that each ran `steps` steps of their own
+    batch: the slowest rank's times (max over ranks) and the throughput of all
+    ranks' tokens over that time.  Returns (ms, e2e_ms, tokens, tokens_per_s)."""
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    tokens = tokens_per_step * steps * world
+    return ms, e2e_ms, tokens, tokens / (ms / 1e3)
+
+
 # ---------------------------------------------------------------- the GPU arm
 def run_gpu(args, rank, world):
     cfg = workload(args.workload, args.T, args.E)
@@ -286,15 +298,9 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1)
 
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms, tokens, value = aggregate_ranks(ms, e2e_ms, cfg.T, args.steps, world, dev)
     if rank != 0:
         return None
-
-    tokens = cfg.T * args.steps * world
-    value = tokens / (ms / 1e3)
     pk, src = peaks()
     F, B = layer_work(cfg, n_active_routed)
     step_s = ms / 1e3 / args.steps
