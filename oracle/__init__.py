@@ -64,6 +64,9 @@ def _load():
     lib.oracle_widen.argtypes = [vp, i32, ctypes.c_size_t, vp]
     lib.oracle_expert_rows.argtypes = [i32, i32, i32, vp, i32, vp, vp, vp, i32, vp, vp, i32]
     lib.oracle_combine.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp, vp]
+    lib.oracle_combine_partial.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp,
+                                           vp]
+    lib.oracle_combine_partial.restype = ctypes.c_int
     for f in ("oracle_router_scores", "oracle_route", "oracle_plan", "oracle_forward",
               "oracle_forward_sharded", "oracle_max_threads", "oracle_expert_rows",
               "oracle_combine"):
@@ -309,6 +312,30 @@ def combine(rows, slot_row, k, S, w=None, residual=None):
                             y.ctypes.data)
     _check(rc, "oracle_combine")
     return y
+
+
+def combine_partial(rows, slot_row, ids, w, avail, k, S, E, residual=None):
+    """Combine with unavailable experts: (y [T, d] fp64, missing [T, k+S] int32).
+
+    avail[e] (e < E+S) is nonzero for experts that responded; responding routed
+    slots keep the token's routed gate mass (w * mass / resp), unavailable slots
+    and shared experts drop out and are reported in `missing`."""
+    lib = _load()
+    rows = _f64(rows)
+    sr = np.ascontiguousarray(slot_row, dtype=np.int32)
+    idv = np.ascontiguousarray(ids, dtype=np.int32)
+    wv = _f64(w)
+    av = np.ascontiguousarray(avail, dtype=np.int32)
+    res = _f64(residual)
+    T = sr.shape[0]
+    d = rows.shape[1]
+    y = np.empty((T, d), np.float64)
+    missing = np.empty((T, k + S), np.int32)
+    rc = lib.oracle_combine_partial(T, d, k, S, E, rows.ctypes.data, sr.ctypes.data,
+                                    idv.ctypes.data, wv.ctypes.data, av.ctypes.data, _ptr(res),
+                                    y.ctypes.data, missing.ctypes.data)
+    _check(rc, "oracle_combine_partial")
+    return y, missing
 
 
 def widen(a):

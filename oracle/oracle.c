@@ -498,6 +498,49 @@ int oracle_combine(int T, int d, int k, int S, const double* rows, const int32_t
   return OR_OK;
 }
 
+/* -------------------------------------------------------------------------
+ * Partial combine ("Distributed MoE", failover paragraph: with allow_partial
+ * a forward that cannot cover every (expert, token) pair renormalises the
+ * gate weights over the experts that responded and reports the unserved
+ * pairs as missing -- a reduced top-k).
+ * Reading taken: avail[e] (e < E+S) says whether expert e responded.  For
+ * token t, with mass = sum_{j<k} w_tj and resp = sum_{j<k, avail} w_tj, each
+ * responding routed slot gets w_tj * mass / resp (the token keeps its routed
+ * gate mass; nothing missing => the plain combine); a token none of whose
+ * routed experts responded gets no routed term.  A shared expert that did
+ * not respond is dropped (weight 0).  missing[t, j] = 1 for every slot whose
+ * expert did not respond, else 0.
+ * ------------------------------------------------------------------------- */
+int oracle_combine_partial(int T, int d, int k, int S, int E, const double* rows,
+                           const int32_t* slot_row, const int32_t* ids, const double* w,
+                           const int32_t* avail, const double* residual, double* y,
+                           int32_t* missing) {
+  if (T < 0 || d <= 0 || k <= 0 || S < 0 || E <= 0 || !w || !ids || !avail) return OR_EINVAL;
+  const int ks = k + S;
+  for (int t = 0; t < T; ++t) {
+    double mass = 0.0, resp = 0.0;
+    for (int j = 0; j < k; ++j) {
+      const double wj = w[(size_t)t * k + j];
+      mass += wj;
+      if (avail[ids[(size_t)t * k + j]]) resp += wj;
+    }
+    double* yt = y + (size_t)t * d;
+    for (int m = 0; m < d; ++m) yt[m] = 0.0;
+    for (int j = 0; j < ks; ++j) {
+      const int e = j < k ? ids[(size_t)t * k + j] : E + (j - k);
+      const int ok = avail[e] != 0;
+      if (missing) missing[(size_t)t * ks + j] = ok ? 0 : 1;
+      if (!ok) continue;
+      const double wj = j < k ? w[(size_t)t * k + j] * (mass / resp) : 1.0;
+      const int32_t r = slot_row[(size_t)t * ks + j];
+      for (int m = 0; m < d; ++m) yt[m] += wj * rows[(size_t)r * d + m];
+    }
+    if (residual)
+      for (int m = 0; m < d; ++m) yt[m] += residual[(size_t)t * d + m];
+  }
+  return OR_OK;
+}
+
 /* Widen a whole fp32/bf16 array to fp64 (used by the tests to read stored values). */
 void oracle_widen(const void* src, int dt, size_t n, double* dst) {
   for (size_t i = 0; i < n; ++i) dst[i] = widen(src, dt, i);

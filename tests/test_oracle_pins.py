@@ -448,3 +448,64 @@ def test_sharded_pieces_compose_to_forward():
     y2 = oracle.combine(rows, p["slot_row"], 2, 1, w=w2)
     np.testing.assert_array_equal(ids, ids2)
     np.testing.assert_allclose(y2, y, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- partial combine
+def _partial_case(seed=3, T=12, k=3, S=1, E=6):
+    rng = np.random.default_rng(seed)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    w = rng.uniform(0.05, 1.0, (T, k))
+    p = oracle.plan(ids, E, S)
+    return rng, ids, w, p
+
+
+def test_partial_combine_with_everyone_responding_is_the_plain_combine():
+    rng, ids, w, p = _partial_case()
+    rows = rng.standard_normal((12 * 4, 10))
+    y, missing = oracle.combine_partial(rows, p["slot_row"], ids, w, np.ones(7), 3, 1, 6)
+    np.testing.assert_array_equal(y, oracle.combine(rows, p["slot_row"], 3, 1, w=w))
+    assert missing.sum() == 0
+
+
+def test_partial_combine_effective_weights():
+    """Unit-vector rows expose every slot's effective weight: unavailable slots
+    weigh 0, responding routed slots w * mass / resp (numpy), so the routed mass
+    sum_j w_j is kept; an unavailable shared expert drops out."""
+    rng, ids, w, p = _partial_case(T=10)
+    P = 10 * 4
+    avail = np.ones(7, np.int32)
+    avail[[1, 4, 6]] = 0  # two routed experts and the shared one are down
+    y, missing = oracle.combine_partial(np.eye(P), p["slot_row"], ids, w, avail, 3, 1, 6)
+    sr = p["slot_row"]
+    for t in range(10):
+        ok = avail[ids[t]] == 1
+        eff = y[t, sr[t, :3]]
+        if ok.any():
+            np.testing.assert_allclose(eff, np.where(ok, w[t] * w[t].sum() / w[t][ok].sum(), 0),
+                                       rtol=1e-14, atol=0)
+            np.testing.assert_allclose(eff.sum(), w[t].sum(), rtol=1e-14)
+        else:
+            assert np.all(eff == 0)
+        assert y[t, sr[t, 3]] == 0.0  # shared expert down
+        np.testing.assert_array_equal(missing[t], np.r_[~ok, True].astype(np.int32))
+
+
+def test_partial_combine_is_a_reduced_top_k():
+    """With the sigmoid family's normalised weights, renormalising over the
+    responding experts gives rs * s_j / sum over responding s (scipy), i.e. the
+    weights of the same routing with the missing experts left out."""
+    rng = np.random.default_rng(8)
+    logits = rng.standard_normal((20, 9))
+    x = np.ascontiguousarray(logits)
+    ids, w = oracle.route(x, np.eye(9), 4, oracle.GATE_SIGMOID, norm_topk=1, routed_scaling=2.5)
+    p = oracle.plan(ids, 9, 0)
+    avail = np.ones(9, np.int32)
+    avail[[0, 5]] = 0
+    y, _ = oracle.combine_partial(np.eye(20 * 4), p["slot_row"], ids, w, avail, 4, 0, 9)
+    s = scipy.special.expit(np.take_along_axis(logits, ids, 1))
+    ok = avail[ids] == 1
+    for t in range(20):
+        if not ok[t].any():
+            continue
+        ref = np.where(ok[t], 2.5 * s[t] / s[t][ok[t]].sum(), 0.0)
+        np.testing.assert_allclose(y[t, p["slot_row"][t]], ref, rtol=1e-13, atol=1e-15)
