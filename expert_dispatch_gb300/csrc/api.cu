@@ -317,6 +317,24 @@ moe_status moe_combine(const moe_layer_desc* desc, const void* y_perm, const int
                                     static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_combine_partial(const moe_layer_desc* desc, const void* y_perm,
+                               const int32_t* slot_row, const int32_t* topk_ids,
+                               const float* topk_w, const int32_t* expert_available,
+                               const float* residual, float* y, int32_t* missing,
+                               void* stream) {
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->T == 0) return MOE_OK;
+  if (!y_perm || !slot_row || !topk_ids || !topk_w || !expert_available || !y)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y) || (residual && !aligned16(residual)))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_combine_partial(desc->dtype, y_perm, slot_row, topk_ids, topk_w,
+                                            expert_available, residual, desc->T, desc->d,
+                                            desc->k, desc->S, desc->E, y, missing,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const void* Wr,
                              const float* logit_bias, const float* sel_bias, const void* Wg,
                              const void* Wu, const void* Wd, const float* residual, float* y,

@@ -118,6 +118,12 @@ cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_ro
                            const float* topk_w, const float* residual, int T, int d, int k,
                            int S, float* y, cudaStream_t s);
 
+cudaError_t launch_combine_partial(int dtype, const void* y_perm, const int32_t* slot_row,
+                                   const int32_t* ids, const float* topk_w,
+                                   const int32_t* avail, const float* residual, int T, int d,
+                                   int k, int S, int E, float* y, int32_t* missing,
+                                   cudaStream_t s);
+
 int num_sms();
 
 }  // namespace moe

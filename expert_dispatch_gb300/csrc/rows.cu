@@ -111,7 +111,101 @@ __global__ void __launch_bounds__(128) combine_kernel(const void* __restrict__ y
   }
 }
 
+// Partial combine ("Distributed MoE", failover paragraph: allow_partial
+// renormalises the gate weights over the experts that responded and reports
+// the unserved pairs).  avail[e] != 0 marks experts that responded.  A
+// responding routed slot weighs w * (mass / resp), with mass the token's
+// routed gate weight sum and resp the responding part, both summed in slot
+// order; unavailable slots (and ids outside [0, E)) weigh 0 and are reported
+// in missing[t, j]; an unavailable shared expert drops out.
+template <bool BF16>
+__global__ void __launch_bounds__(128) combine_partial_kernel(
+    const void* __restrict__ y_perm, const int32_t* __restrict__ slot_row,
+    const int32_t* __restrict__ ids, const float* __restrict__ topk_w,
+    const int32_t* __restrict__ avail, const float* __restrict__ residual, int d, int k, int S,
+    int E, int P, float* __restrict__ y, int32_t* __restrict__ missing) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int rows_s[kCombineMaxSlots];
+  __shared__ float w_s[kCombineMaxSlots];
+  __shared__ float scale_s;
+  const int t = blockIdx.x;
+  const int ks = k + S;
+  if (threadIdx.x < ks) {
+    const int j = threadIdx.x;
+    const int e = j < k ? ids[(size_t)t * k + j] : E + (j - k);
+    const bool ok = e >= 0 && e < E + S && (j >= k || e < E) && avail[e] != 0;
+    const int r = slot_row[(size_t)t * ks + j];
+    rows_s[j] = (!ok || r < 0 || r >= P) ? -1 : r;
+    w_s[j] = j < k ? topk_w[(size_t)t * k + j] : 1.f;
+    if (missing && blockIdx.y == 0) missing[(size_t)t * ks + j] = ok ? 0 : 1;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mass = 0.f, resp = 0.f;
+    for (int j = 0; j < k; ++j) {
+      mass += w_s[j];
+      if (rows_s[j] >= 0) resp += w_s[j];
+    }
+    scale_s = resp > 0.f ? mass / resp : 0.f;
+  }
+  __syncthreads();
+  const int c = blockIdx.y * 1024 + threadIdx.x * 8;
+  if (c >= d) return;
+  const float scale = scale_s;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < ks; ++j) {
+    const int r = rows_s[j];
+    if (r < 0) continue;
+    const float w = j < k ? w_s[j] * scale : 1.f;
+    if (BF16) {
+      add8(acc, *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(y_perm) +
+                                                (size_t)r * d + c),
+           w);
+    } else {
+      const float4* src =
+          reinterpret_cast<const float4*>(static_cast<const float*>(y_perm) + (size_t)r * d + c);
+      const float4 a = src[0], b = src[1];
+      acc[0] = fmaf(w, a.x, acc[0]);
+      acc[1] = fmaf(w, a.y, acc[1]);
+      acc[2] = fmaf(w, a.z, acc[2]);
+      acc[3] = fmaf(w, a.w, acc[3]);
+      acc[4] = fmaf(w, b.x, acc[4]);
+      acc[5] = fmaf(w, b.y, acc[5]);
+      acc[6] = fmaf(w, b.z, acc[6]);
+      acc[7] = fmaf(w, b.w, acc[7]);
+    }
+  }
+  if (residual) {
+    const float4* rs = reinterpret_cast<const float4*>(residual + (size_t)t * d + c);
+    const float4 a = rs[0], b = rs[1];
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+  }
+  float4* dst = reinterpret_cast<float4*>(y + (size_t)t * d + c);
+  dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
 }  // namespace
+
+cudaError_t launch_combine_partial(int dtype, const void* y_perm, const int32_t* slot_row,
+                                   const int32_t* ids, const float* topk_w,
+                                   const int32_t* avail, const float* residual, int T, int d,
+                                   int k, int S, int E, float* y, int32_t* missing,
+                                   cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int P = T * (k + S);
+  ProfScope pr("combine_partial", s);
+  const dim3 grid(T, (d + 1023) / 1024);
+  if (dtype == MOE_BF16)
+    (void)launch_kernel(combine_partial_kernel<true>, grid, 128, 0, s, y_perm, slot_row, ids,
+                        topk_w, avail, residual, d, k, S, E, P, y, missing);
+  else
+    (void)launch_kernel(combine_partial_kernel<false>, grid, 128, 0, s, y_perm, slot_row, ids,
+                        topk_w, avail, residual, d, k, S, E, P, y, missing);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* tok_idx,
                                const int32_t* total_rows, int P, int T, int d, void* x_perm,

@@ -37,7 +37,7 @@ MOE_BF16 = 1
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status",
             "moe_status_string", "moe_launch_count", "moe_profile_enable", "moe_profile_query",
-            "moe_expert_ffn_noalloc")
+            "moe_expert_ffn_noalloc", "moe_combine_partial")
 
 
 class MoeError(RuntimeError):
@@ -93,6 +93,7 @@ def lib():
     L.moe_launch_count.argtypes = []
     L.moe_launch_count.restype = ctypes.c_int64
     L.moe_expert_ffn_noalloc.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_combine_partial.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_profile_enable.argtypes = [i32]
     L.moe_profile_query.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
                                     ctypes.POINTER(ctypes.c_float)]
@@ -243,6 +244,30 @@ def moe_combine(desc, y_perm, slot_row, topk_w, residual, y, stream=None):
                            _p(residual, torch.float32, "residual"), _p(y, torch.float32, "y"),
                            _stream(stream))
     _check(st, "moe_combine")
+
+
+def moe_combine_partial(desc, y_perm, slot_row, topk_ids, topk_w, expert_available, residual, y,
+                        missing=None, stream=None):
+    """Combine when some experts did not respond (expert_available[E+S] int32):
+    weights renormalised over the responding routed experts, unserved slots
+    reported in missing[T, k+S]."""
+    dt = _act_dtype(desc)
+    ks = desc.k + desc.S
+    _need(y_perm, (desc.T * ks, desc.d), "y_perm")
+    _need(slot_row, (desc.T, ks), "slot_row")
+    _need(topk_ids, (desc.T, desc.k), "topk_ids")
+    _need(topk_w, (desc.T, desc.k), "topk_w")
+    _need(expert_available, (desc.E + desc.S,), "expert_available")
+    _need(y, (desc.T, desc.d), "y")
+    if missing is not None:
+        _need(missing, (desc.T, ks), "missing")
+    st = lib().moe_combine_partial(
+        ctypes.byref(desc), _p(y_perm, dt, "y_perm"), _p(slot_row, torch.int32, "slot_row"),
+        _p(topk_ids, torch.int32, "topk_ids"), _p(topk_w, torch.float32, "topk_w"),
+        _p(expert_available, torch.int32, "expert_available"),
+        _p(residual, torch.float32, "residual"), _p(y, torch.float32, "y"),
+        _p(missing, torch.int32, "missing"), _stream(stream))
+    _check(st, "moe_combine_partial")
 
 
 def moe_layer_forward(desc, x, Wr, logit_bias, sel_bias, Wg, Wu, Wd, residual, y, topk_ids_out,

@@ -188,6 +188,28 @@ moe_status moe_expert_ffn_noalloc(const moe_layer_desc* desc, const void* x,
 moe_status moe_combine(const moe_layer_desc* desc, const void* y_perm, const int32_t* slot_row,
                        const float* topk_w, const float* residual, float* y, void* stream);
 
+/* moe_combine_partial -- the combine when some experts did not respond
+   ("Distributed MoE", failover paragraph: allow_partial renormalises the gate
+   weights over the experts that responded and reports the unserved
+   (expert, token) pairs as missing -- serving with a reduced top-k).
+     topk_ids         [T, k] int32 and topk_w [T, k] fp32: the routing.
+     expert_available [E+S] int32: nonzero for experts whose rows in y_perm
+                      are valid (rows of the others are never read).
+     missing          [T, k+S] int32 out (or NULL): 1 for every slot whose
+                      expert was unavailable, else 0.
+   For token t, mass = sum_j topk_w[t, j] and resp = the same sum over the
+   available routed slots (slot order, fp32); an available routed slot
+   weighs topk_w[t, j] * (mass / resp), so the token keeps its routed gate
+   mass and, with every expert available, the result is moe_combine's
+   exactly.  A token with no available routed expert gets no routed term;
+   an unavailable shared expert is left out.  y and residual as in
+   moe_combine; y_perm rows must not be pre-weighted. */
+moe_status moe_combine_partial(const moe_layer_desc* desc, const void* y_perm,
+                               const int32_t* slot_row, const int32_t* topk_ids,
+                               const float* topk_w, const int32_t* expert_available,
+                               const float* residual, float* y, int32_t* missing,
+                               void* stream);
+
 /* moe_layer_forward -- gate -> plan -> expert FFN -> combine ("Distributed
    MoE", RPC list: forward).  topk_ids_out [T, k] / topk_w_out [T, k] may be
    NULL; everything else as in the calls above.                             */
@@ -214,8 +236,8 @@ int64_t moe_launch_count(void);
    synchronizes on the recorded events and returns, for the named kernel, the
    number of recorded launches and their summed device time in milliseconds.
    Kernel names: router_logits_splitk, router_logits_tc, router_topk,
-   plan_mark, plan_scan, plan_place, gather_rows, ffn_gateup_simt,
-   ffn_down_simt, ffn_gateup_tc, ffn_down_tc, combine.                      */
+   plan_small, plan_mark, plan_scan, plan_place, gather_rows, ffn_gateup_simt,
+   ffn_down_simt, ffn_gateup_tc, ffn_down_tc, combine, combine_partial.      */
 moe_status moe_profile_enable(int on);
 moe_status moe_profile_query(const char* kernel, int32_t* launches, float* total_ms);
 

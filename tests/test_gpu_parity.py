@@ -298,3 +298,43 @@ def test_full_skewed_zipf():
 @pytest.mark.parametrize("T", DECODE_TS)
 def test_full_kimi_decode(T):
     _full_size(KIMI_DECODE.with_T(T), n_sample=8)
+
+
+# ---------------------------------------------------------------- partial combine
+@pytest.mark.parametrize("cfg", [FFN_CASES[2], FFN_CASES[1], ROUTER_CASES[3]],
+                         ids=lambda c: c.name)
+def test_combine_partial_parity(cfg):
+    """The partial combine against the oracle, with routed experts (and, where
+    present, the shared expert) unavailable; all available = moe_combine exactly."""
+    inp = _case(cfg, seed=21)
+    ids, w = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
+                          **_oracle_kw(cfg, inp))
+    plan = oracle.plan(ids, cfg.E, cfg.S)
+    desc = moe.desc_from_config(cfg)
+    P = cfg.T * (cfg.k + cfg.S)
+    g = torch.Generator(device=DEV).manual_seed(4)
+    y_perm = torch.randn((P, cfg.d), generator=g, device=DEV).to(cfg.torch_dtype)
+    rows = host(y_perm).double().numpy()
+    sr = torch.from_numpy(plan["slot_row"]).to(DEV)
+    g_ids = torch.from_numpy(ids).to(DEV)
+    w32 = w.astype(np.float32)
+    g_w = torch.from_numpy(w32).to(DEV)
+    avail = np.ones(cfg.E + cfg.S, np.int32)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=DEV)
+    y_ref_full = torch.empty_like(y)
+    miss = torch.full((cfg.T, cfg.k + cfg.S), 7, dtype=torch.int32, device=DEV)
+    moe.moe_combine_partial(desc, y_perm, sr, g_ids, g_w, torch.from_numpy(avail).to(DEV), None,
+                            y, miss)
+    moe.moe_combine(desc, y_perm, sr, g_w, None, y_ref_full)
+    assert torch.equal(y, y_ref_full) and int(miss.sum()) == 0
+    rng = np.random.default_rng(1)
+    avail[rng.choice(cfg.E, size=max(1, cfg.E // 3), replace=False)] = 0
+    if cfg.S:
+        avail[cfg.E] = 0
+    res = torch.randn((cfg.T, cfg.d), generator=g, device=DEV)
+    moe.moe_combine_partial(desc, y_perm, sr, g_ids, g_w, torch.from_numpy(avail).to(DEV), res,
+                            y, miss)
+    y_ref, miss_ref = oracle.combine_partial(rows, plan["slot_row"], ids, w32, avail, cfg.k,
+                                             cfg.S, cfg.E, residual=host(res))
+    np.testing.assert_array_equal(host(miss).numpy(), miss_ref)
+    assert rel_err(host(y).numpy(), y_ref) <= 1e-6
