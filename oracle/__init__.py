@@ -67,6 +67,10 @@ def _load():
     lib.oracle_combine_partial.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp,
                                            vp]
     lib.oracle_combine_partial.restype = ctypes.c_int
+    lib.oracle_quantize_q8_0.argtypes = [i32, i32, i32, i32, vp, vp, vp]
+    lib.oracle_quantize_q8_0.restype = ctypes.c_int
+    lib.oracle_dequantize_q8_0.argtypes = [i32, i32, i32, vp, vp, vp]
+    lib.oracle_dequantize_q8_0.restype = ctypes.c_int
     for f in ("oracle_router_scores", "oracle_route", "oracle_plan", "oracle_forward",
               "oracle_forward_sharded", "oracle_max_threads", "oracle_expert_rows",
               "oracle_combine"):
@@ -336,6 +340,31 @@ def combine_partial(rows, slot_row, ids, w, avail, k, S, E, residual=None):
                                     y.ctypes.data, missing.ctypes.data)
     _check(rc, "oracle_combine_partial")
     return y, missing
+
+
+def quantize_q8_0(w):
+    """Q8_0 codes and scales of w [n_mats, R, K] (fp32 or bf16 host tensor):
+    (q int8 [n_mats, R, K], scales uint16 (f16 bits) [n_mats, K/32, R])."""
+    lib = _load()
+    wa = _Arr(w)
+    n, R, K = wa.shape
+    q = np.empty((n, R, K), np.int8)
+    s = np.empty((n, K // 32, R), np.uint16)
+    _check(lib.oracle_quantize_q8_0(n, R, K, wa.dt, wa.ptr, q.ctypes.data, s.ctypes.data),
+           "oracle_quantize_q8_0")
+    return q, s
+
+
+def dequantize_q8_0(q, scales):
+    """scale * q in fp64, [n_mats, R, K] (exact)."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    s = np.ascontiguousarray(scales, dtype=np.uint16)
+    n, R, K = q.shape
+    out = np.empty((n, R, K), np.float64)
+    _check(lib.oracle_dequantize_q8_0(n, R, K, q.ctypes.data, s.ctypes.data, out.ctypes.data),
+           "oracle_dequantize_q8_0")
+    return out
 
 
 def widen(a):

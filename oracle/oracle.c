@@ -541,6 +541,64 @@ int oracle_combine_partial(int T, int d, int k, int S, int E, const double* rows
   return OR_OK;
 }
 
+/* -------------------------------------------------------------------------
+ * Q8_0 block quantization ("Distributed MoE", quantization table: 32-element
+ * blocks with one f16 scale, about 8.5 bits per weight; the prepare job
+ * block-quantizes each expert projection).
+ * For every block of 32 consecutive elements along K of a row:
+ *   amax = max |w|;  d = amax / 127 (fp32);  id = d != 0 ? 1 / d : 0 (fp32);
+ *   q[i] = round-half-away(w[i] * id) (fp32 product);  scale = f16(d) (to nearest even).
+ * The block represents scale * q[i].  Codes keep the weight's layout
+ * q[m][r][k]; scales are stored transposed per matrix, s[m][k/32][r].
+ * (Reading: the codes are decided in fp32 from the unrounded d, and f16(d)
+ * is what is stored, as GGUF-style encoders do.)
+ * ------------------------------------------------------------------------- */
+int oracle_quantize_q8_0(int n_mats, int R, int K, int w_dt, const void* w, int8_t* q,
+                         uint16_t* scales) {
+  if (n_mats < 0 || R <= 0 || K <= 0 || K % 32) return OR_EINVAL;
+  const int nb = K / 32;
+  for (int m = 0; m < n_mats; ++m)
+    for (int r = 0; r < R; ++r)
+      for (int b = 0; b < nb; ++b) {
+        const size_t base = ((size_t)m * R + r) * K + (size_t)b * 32;
+        float v[32];
+        float amax = 0.0f;
+        for (int i = 0; i < 32; ++i) {
+          v[i] = (float)widen(w, w_dt, base + (size_t)i);
+          const float a = fabsf(v[i]);
+          if (a > amax) amax = a;
+        }
+        const float d = amax / 127.0f;
+        const float id = d != 0.0f ? 1.0f / d : 0.0f;
+        for (int i = 0; i < 32; ++i) {
+          const float prod = v[i] * id;
+          q[base + (size_t)i] = (int8_t)roundf(prod);
+        }
+        const _Float16 dh = (_Float16)d;
+        uint16_t bits;
+        memcpy(&bits, &dh, sizeof bits);
+        scales[((size_t)m * nb + b) * R + r] = bits;
+      }
+  return OR_OK;
+}
+
+/* scale * q as fp64 (exact), out[m][r][k] */
+int oracle_dequantize_q8_0(int n_mats, int R, int K, const int8_t* q, const uint16_t* scales,
+                           double* out) {
+  if (n_mats < 0 || R <= 0 || K <= 0 || K % 32) return OR_EINVAL;
+  const int nb = K / 32;
+  for (int m = 0; m < n_mats; ++m)
+    for (int r = 0; r < R; ++r)
+      for (int k = 0; k < K; ++k) {
+        _Float16 dh;
+        const uint16_t bits = scales[((size_t)m * nb + k / 32) * R + r];
+        memcpy(&dh, &bits, sizeof dh);
+        const size_t i = ((size_t)m * R + r) * K + k;
+        out[i] = (double)(float)dh * (double)q[i];
+      }
+  return OR_OK;
+}
+
 /* Widen a whole fp32/bf16 array to fp64 (used by the tests to read stored values). */
 void oracle_widen(const void* src, int dt, size_t n, double* dst) {
   for (size_t i = 0; i < n; ++i) dst[i] = widen(src, dt, i);

@@ -509,3 +509,46 @@ def test_partial_combine_is_a_reduced_top_k():
             continue
         ref = np.where(ok[t], 2.5 * s[t] / s[t][ok[t]].sum(), 0.0)
         np.testing.assert_allclose(y[t, p["slot_row"][t]], ref, rtol=1e-13, atol=1e-15)
+
+
+# ---------------------------------------------------------------- Q8_0 weights
+def test_q8_0_round_trip_is_exact_on_representable_blocks():
+    """Blocks of the form s * q (s an f16 value, integer codes with max |q| = 127)
+    quantize back to exactly those codes and that scale."""
+    rng = np.random.default_rng(0)
+    n, R, K = 2, 5, 96
+    q0 = rng.integers(-127, 128, size=(n, R, K)).astype(np.int8)
+    q0[..., ::32] = 127 * rng.choice([-1, 1], size=(n, R, K // 32))  # a code of |127| per block
+    s0 = rng.uniform(1e-3, 5e-2, size=(n, K // 32, R)).astype(np.float16)
+    w = (s0.astype(np.float64).transpose(0, 2, 1).repeat(32, axis=2) * q0).astype(np.float32)
+    q, s = oracle.quantize_q8_0(torch.from_numpy(w))
+    np.testing.assert_array_equal(q, q0)
+    np.testing.assert_array_equal(s, s0.view(np.uint16))
+    np.testing.assert_array_equal(oracle.dequantize_q8_0(q, s), w.astype(np.float64))
+
+
+def test_q8_0_error_bound_and_special_blocks():
+    """|w - scale*q| <= d/2 + 127 |d - f16(d)| (d = amax/127) elementwise; max |q| is
+    127 in every nonzero block; an all-zero block has scale 0 and codes 0; negating
+    the input negates the codes; the scale is the f16 nearest to amax/127."""
+    g = torch.Generator().manual_seed(5)
+    w = (torch.randn(3, 7, 128, generator=g) * 0.02).to(torch.bfloat16)
+    w[1, 2, 32:64] = 0
+    q, s = oracle.quantize_q8_0(w)
+    wf = w.double().numpy()
+    blocks = wf.reshape(3, 7, 4, 32)
+    d = np.abs(blocks).max(-1) / 127.0                       # [3, 7, 4]
+    sd = s.view(np.float16).astype(np.float64).transpose(0, 2, 1)  # [3, 7, 4]
+    err = np.abs(wf - oracle.dequantize_q8_0(q, s)).reshape(3, 7, 4, 32)
+    bound = d / 2 + 127 * np.abs(d - sd) + 1e-12
+    assert np.all(err <= bound[..., None])
+    qb = np.abs(q.astype(np.int32)).reshape(3, 7, 4, 32).max(-1)
+    nz = d > 0
+    assert np.all(qb[nz] == 127) and np.all(qb[~nz] == 0) and np.all(sd[~nz] == 0)
+    ulp = np.spacing(np.abs(d).astype(np.float16)).astype(np.float64)
+    assert np.all(np.abs(sd - d) <= ulp / 2 + 1e-18)
+    qn, sn = oracle.quantize_q8_0(-w)
+    np.testing.assert_array_equal(qn, -q)
+    np.testing.assert_array_equal(sn, s)
+    # 32 int8 codes + one f16 scale per block: 8.5 bits per weight
+    assert (q.nbytes + s.nbytes) * 8 / q.size == 8.5
