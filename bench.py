@@ -41,7 +41,7 @@ PUBLISHED_CONTEXT = ("53k tok/s per worker at batch 512 on ROCm hardware, expert
                      "precision unstated (context only, not the same workload)")
 KERNELS = ("router_logits_splitk", "router_logits_tc", "router_topk", "plan_small", "plan_mark",
            "plan_scan", "plan_place", "gather_rows", "ffn_gateup_simt", "ffn_down_simt", "ffn_gateup_tc",
-           "ffn_down_tc", "combine")
+           "ffn_down_tc", "ffn_gateup_tc_q8", "ffn_down_tc_q8", "combine")
 
 
 def workload(name, T=None, E=None):
@@ -136,13 +136,17 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- algorithmic work
-def layer_work(cfg, n_active_routed):
+Q8_BYTES_PER_WEIGHT = 34 / 32  # 32 int8 codes + one f16 scale per block
+
+
+def layer_work(cfg, n_active_routed, weights="dense"):
     """F (flop) and B (bytes) of one layer call, per the hot-path scope table:
     router + expert flops; active weights + router + x + fp32 y bytes."""
     P = cfg.T * cfg.k
     bw = bx = 2 if cfg.dtype == "bf16" else 4
+    bexp = Q8_BYTES_PER_WEIGHT if weights == "q8_0" else bw
     F = 2.0 * cfg.T * cfg.d * cfg.E + 6.0 * cfg.d * cfg.I * (P + cfg.S * cfg.T)
-    B = ((n_active_routed * 3 * cfg.d * cfg.I + cfg.S * 3 * cfg.d * cfg.I) * bw
+    B = ((n_active_routed * 3 * cfg.d * cfg.I + cfg.S * 3 * cfg.d * cfg.I) * bexp
          + cfg.E * cfg.d * bw + cfg.T * cfg.d * bx + cfg.T * cfg.d * 4)
     return F, B
 
@@ -152,10 +156,11 @@ def kernel_bytes(cfg, kernel, n_active_all):
     streams plus the rows it must read and write once."""
     P = cfg.T * (cfg.k + cfg.S)
     es = 2 if cfg.dtype == "bf16" else 4
-    if kernel in ("ffn_gateup_tc", "ffn_gateup_simt"):
-        return n_active_all * 2 * cfg.I * cfg.d * es + P * cfg.d * es + P * cfg.I * es
-    if kernel in ("ffn_down_tc", "ffn_down_simt"):
-        return n_active_all * cfg.d * cfg.I * es + P * cfg.I * es + P * cfg.d * es
+    ew = Q8_BYTES_PER_WEIGHT if kernel.endswith("_q8") else es
+    if kernel in ("ffn_gateup_tc", "ffn_gateup_simt", "ffn_gateup_tc_q8"):
+        return n_active_all * 2 * cfg.I * cfg.d * ew + P * cfg.d * es + P * cfg.I * es
+    if kernel in ("ffn_down_tc", "ffn_down_simt", "ffn_down_tc_q8"):
+        return n_active_all * cfg.d * cfg.I * ew + P * cfg.I * es + P * cfg.d * es
     return None
 
 
@@ -200,8 +205,11 @@ def run_gpu(args, rank, world):
         torch.distributed.barrier()
     inp = make_inputs(cfg, seed=args.seed + rank, device=dev)
     desc = moe.desc_from_config(cfg)
-    layer = moe.MoeLayer(desc, inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"],
-                         logit_bias=inp["logit_bias"], sel_bias=inp["sel_bias"])
+    Wg, Wu, Wd = inp["Wg"], inp["Wu"], inp["Wd"]
+    if args.weights == "q8_0":  # the prepare step, once, outside any timing
+        Wg, Wu, Wd = (moe.quantize_q8_0(W) for W in (Wg, Wu, Wd))
+    layer = moe.MoeLayer(desc, inp["Wr"], Wg, Wu, Wd, logit_bias=inp["logit_bias"],
+                         sel_bias=inp["sel_bias"])
     x = inp["x"]
     y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
     ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
@@ -302,7 +310,7 @@ def run_gpu(args, rank, world):
     if rank != 0:
         return None
     pk, src = peaks()
-    F, B = layer_work(cfg, n_active_routed)
+    F, B = layer_work(cfg, n_active_routed, args.weights)
     step_s = ms / 1e3 / args.steps
     t_star = max(F / (pk["bf16_tflops"] * 1e12), B / (pk["hbm_gbs"] * 1e9))
     total_kernel_ms = sum(v["ms_per_launch"] * v["launches"] for v in per_kernel.values())
@@ -319,7 +327,7 @@ def run_gpu(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
         "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "I": cfg.I,
-                   "k": cfg.k, "shared": cfg.S,
+                   "k": cfg.k, "shared": cfg.S, "expert_weights": args.weights,
                    "gate": "softmax" if cfg.gate == 0 else "sigmoid+bias",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: each step streams %.1f GB of expert weights"
@@ -342,7 +350,7 @@ def run_gpu(args, rank, world):
         "clocks": clocks,
         "published_context": PUBLISHED_CONTEXT,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and args.weights == "dense":
         out["cpu_baseline"] = cpu_baseline(cfg, inp, budget_s=args.cpu_budget)
     return out
 
@@ -430,6 +438,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", default="dense", choices=("dense", "q8_0"),
+                    help="expert weights in the layer's dtype, or Q8_0 blocks")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time direct launches instead of CUDA-graph replays")
     args = ap.parse_args()

@@ -150,6 +150,25 @@ moe_status do_ffn(const moe_layer_desc* D, const void* x, const int32_t* offsets
   return cuda_status(e);
 }
 
+// The same with Q8_0 expert weights (bf16 activations).
+moe_status do_ffn_q8(const moe_layer_desc* D, const void* x, const int32_t* offsets,
+                     const int32_t* tok_idx, const float* slot_w, const moe_q8_weight* Wg,
+                     const moe_q8_weight* Wu, const moe_q8_weight* Wd, void* y_perm, const Ws& W,
+                     cudaStream_t s) {
+  const int P = D->T * (D->k + D->S);
+  const int nE = D->E + D->S;
+  if (launch_gather_rows_to_f16(x, tok_idx, offsets + nE, P, D->T, D->d, W.x_perm, W.flags, s) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  const Q8Weight g{Wg->q, Wg->scale}, u{Wu->q, Wu->scale}, dn{Wd->q, Wd->scale};
+  return cuda_status(launch_ffn_tc_q8(W.x_perm, offsets, nE, P, D->d, D->I, (double)P / nE, g, u,
+                                      dn, slot_w, W.h, y_perm, W.flags, s));
+}
+
+bool q8_ok(const moe_q8_weight* w) {
+  return w && w->q && w->scale && aligned16(w->q) && aligned16(w->scale);
+}
+
 }  // namespace
 
 RouterPlan router_plan(int dtype, int T, int d, int E) {
@@ -315,6 +334,68 @@ moe_status moe_combine(const moe_layer_desc* desc, const void* y_perm, const int
   return cuda_status(launch_combine(desc->dtype, y_perm, slot_row, topk_w, residual, desc->T,
                                     desc->d, desc->k, desc->S, y,
                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_quantize_q8_0(int n_mats, int rows, int K, int src_dtype, const void* w, void* q,
+                             void* scale, void* stream) {
+  if (n_mats < 0 || rows <= 0 || K <= 0 || K % 32) return MOE_ERR_INVALID_ARG;
+  if (src_dtype != MOE_F32 && src_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (n_mats == 0) return MOE_OK;
+  if (!w || !q || !scale) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_q8_0(src_dtype, w, n_mats, rows, K,
+                                          static_cast<int8_t*>(q), static_cast<uint16_t*>(scale),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_expert_ffn_q8(const moe_layer_desc* desc, const void* x,
+                             const int32_t* expert_offsets, const int32_t* token_indices,
+                             const float* slot_w, const moe_q8_weight* Wg,
+                             const moe_q8_weight* Wu, const moe_q8_weight* Wd, void* y_perm,
+                             void* workspace, size_t ws_bytes, void* stream) {
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !expert_offsets || !token_indices || !y_perm || !q8_ok(Wg) || !q8_ok(Wu) ||
+      !q8_ok(Wd) || !aligned16(x) || !aligned16(y_perm))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
+  const Ws W = carve(workspace, ws_layout(*desc));
+  return do_ffn_q8(desc, x, expert_offsets, token_indices, slot_w, Wg, Wu, Wd, y_perm, W,
+                   static_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_layer_forward_q8(const moe_layer_desc* desc, const void* x, const void* Wr,
+                                const float* logit_bias, const float* sel_bias,
+                                const moe_q8_weight* Wg, const moe_q8_weight* Wu,
+                                const moe_q8_weight* Wd, const float* residual, float* y,
+                                int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                                size_t ws_bytes, void* stream) {
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !Wr || !y || !q8_ok(Wg) || !q8_ok(Wu) || !q8_ok(Wd)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wr) || !aligned16(y) || (residual && !aligned16(residual)) ||
+      (topk_ids_out && !aligned16(topk_ids_out)) || (topk_w_out && !aligned16(topk_w_out)))
+    return MOE_ERR_INVALID_ARG;
+  if (sel_bias && desc->gate != MOE_GATE_SIGMOID_BIAS) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Ws W = carve(workspace, ws_layout(*desc));
+  int32_t* ids = topk_ids_out ? topk_ids_out : W.topk_ids;
+  float* w = topk_w_out ? topk_w_out : W.topk_w;
+  if (cudaMemsetAsync(W.flags, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((st = do_route(desc, x, Wr, logit_bias, sel_bias, ids, w, W, s)) != MOE_OK) return st;
+  if (launch_plan(ids, nullptr, desc->T, desc->E, desc->k, desc->S, W.offsets, W.tok_idx,
+                  W.slot_row, W.active, W.n_active, nullptr, W.bits, W.wpre, W.counts, W.flags,
+                  s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((st = do_ffn_q8(desc, x, W.offsets, W.tok_idx, nullptr, Wg, Wu, Wd, W.y_perm, W, s)) !=
+      MOE_OK)
+    return st;
+  return cuda_status(launch_combine(desc->dtype, W.y_perm, W.slot_row, w, residual, desc->T,
+                                    desc->d, desc->k, desc->S, y, s));
 }
 
 moe_status moe_combine_partial(const moe_layer_desc* desc, const void* y_perm,

@@ -75,14 +75,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// try_wait with a suspend-time hint: a waiting thread sleeps in hardware until
+// the phase completes (or the hint, in ns, elapses) instead of spinning, so
+// idle warps leave the issue slots to the warps doing work.
+constexpr uint32_t kSuspendHintNs = 100000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -187,6 +192,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   desc |= static_cast<uint64_t>(1) << 46;                    // descriptor version
   desc |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
   return desc;
+}
+
+// Instruction descriptor, kind::f16: fp16 A and B (K-major), fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                                  // D format: f32 (A, B format 0: f16)
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M x N.

@@ -99,6 +99,11 @@ cudaError_t launch_plan(const int32_t* ids, const float* topk_w, int T, int E, i
                         int32_t* n_active, float* slot_w, uint32_t* bits, int32_t* wpre,
                         int32_t* counts, int* flags, cudaStream_t s);
 
+// bf16 rows gathered into fp16 rows (operands of the Q8_0 GEMMs)
+cudaError_t launch_gather_rows_to_f16(const void* x, const int32_t* tok_idx,
+                                      const int32_t* total_rows, int P, int T, int d,
+                                      void* x_perm, int* flags, cudaStream_t s);
+
 cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* tok_idx,
                                const int32_t* total_rows, int P, int T, int d, void* x_perm,
                                int* flags, cudaStream_t s);
@@ -117,6 +122,18 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
 cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_row,
                            const float* topk_w, const float* residual, int T, int d, int k,
                            int S, float* y, cudaStream_t s);
+
+// Q8_0 expert weights: int8 codes [E+S, R, K] and f16 scales [E+S, K/32, R].
+struct Q8Weight {
+  const void* q;
+  const void* scale;
+};
+cudaError_t launch_quantize_q8_0(int dtype, const void* w, int n_mats, int R, int K, int8_t* q,
+                                 uint16_t* scales, cudaStream_t s);
+cudaError_t launch_ffn_tc_q8(const void* x_perm, const int32_t* offsets, int n_groups, int P,
+                             int d, int I, double mean_rows, const Q8Weight& Wg,
+                             const Q8Weight& Wu, const Q8Weight& Wd, const float* slot_w,
+                             void* h, void* y_perm, int* err, cudaStream_t s);
 
 cudaError_t launch_combine_partial(int dtype, const void* y_perm, const int32_t* slot_row,
                                    const int32_t* ids, const float* topk_w,

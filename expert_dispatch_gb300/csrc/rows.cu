@@ -40,6 +40,44 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* _
   for (int v = lane; v < vec_per_row; v += 32) dst[v] = src[v];
 }
 
+// The same gather from bf16 rows into fp16 rows (the operand type of the
+// Q8_0 GEMMs).  A bf16 value converts exactly when it lies in fp16's range;
+// one beyond it (|x| > 65504) is flagged as an input error.
+__global__ void gather_rows_to_f16_kernel(const uint4* __restrict__ x,
+                                          const int32_t* __restrict__ tok,
+                                          const int32_t* __restrict__ total_rows, int P, int T,
+                                          int vec_per_row, uint4* __restrict__ x_perm,
+                                          int* flags) {
+  pdl_wait();
+  pdl_trigger();
+  const int r = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= P || r >= *total_rows) return;
+  const int t = tok[r];
+  if (t < 0 || t >= T) {
+    if (lane == 0) flag_error(flags, kErrDeviceInput);
+    return;
+  }
+  const uint4* src = x + (size_t)t * vec_per_row;
+  uint4* dst = x_perm + (size_t)r * vec_per_row;
+  bool overflow = false;
+  for (int v = lane; v < vec_per_row; v += 32) {
+    const uint4 in = src[v];
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&in);
+    uint4 out;
+    uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(b[i]);
+      overflow |= fabsf(f.x) > 65504.f || fabsf(f.y) > 65504.f;
+      const __half2 h = __floats2half2_rn(f.x, f.y);
+      o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    dst[v] = out;
+  }
+  if (__any_sync(0xffffffffu, overflow) && lane == 0) flag_error(flags, kErrDeviceInput);
+}
+
 __device__ __forceinline__ void add8(float (&acc)[8], uint4 v, float w) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
@@ -204,6 +242,17 @@ cudaError_t launch_combine_partial(int dtype, const void* y_perm, const int32_t*
   else
     (void)launch_kernel(combine_partial_kernel<false>, grid, 128, 0, s, y_perm, slot_row, ids,
                         topk_w, avail, residual, d, k, S, E, P, y, missing);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows_to_f16(const void* x, const int32_t* tok_idx,
+                                      const int32_t* total_rows, int P, int T, int d,
+                                      void* x_perm, int* flags, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  ProfScope pr("gather_rows", s);
+  (void)launch_kernel(gather_rows_to_f16_kernel, (P + 7) / 8, 256, 0, s,
+                      static_cast<const uint4*>(x), tok_idx, total_rows, P, T, d / 8,
+                      static_cast<uint4*>(x_perm), flags);
   return cudaGetLastError();
 }
 

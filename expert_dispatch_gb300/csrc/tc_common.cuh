@@ -1,0 +1,234 @@
+// tc_common.cuh -- pieces shared by the tcgen05 grouped GEMMs (bf16 weights in
+// tc_gemm.cu, Q8_0 weights in tc_gemm_q8.cu): work-unit schedule, bounded
+// waits, the TMEM epilogue, and tensor-map encoding.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2;
+constexpr int kMaxGroups = 1028;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quarter
+
+struct Params {
+  const int32_t* offsets;  // [n_groups + 1] batch boundaries, or null
+  int n_groups;
+  int rows_single;         // rows of the single group when offsets is null
+  int Mg;                  // weight rows per group
+  int K;                   // reduction length (multiple of 64)
+  void* out;
+  int ldo;                 // output row stride, elements
+  const float* row_scale;  // MODE_DOWN: per-row factor or null
+  int* err;
+  int max_rows;            // rows of the token operand / output; batch bounds are clamped to it
+  int ksplit;              // MODE_ROUTER: K is cut into ksplit chunks of kb_per 64-wide blocks,
+  int kb_per;              //   each chunk's partial sums go to out + chunk * rows * ldo
+};
+
+struct Unit {
+  int g, mt, r0, nt, kb0, kb1;
+};
+
+// Unit u -> (group, weight block, token rows, K range).  A group with at most
+// four token tiles is ordered token-tile-minor (a weight block's tiles run
+// back to back, so its bytes come from HBM once); a group with more is
+// ordered weight-block-minor (the CTAs running together cover all weight
+// blocks of a few token tiles, so the expert's weights and those token rows
+// stay in L2 while its tiles are swept).  The router always uses the latter.
+template <int MODE, int BN>
+__device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int* gstart,
+                                            int n_groups, int m_tiles, int KB, const Params& p) {
+  int lo = 0, hi = n_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
+  }
+  const int local = u - prefix[lo];
+  const int cnt = gstart[lo + 1] - gstart[lo];
+  const int tiles = (cnt + BN - 1) / BN;
+  int mt, tt, ks = 0;
+  if (MODE == MODE_ROUTER) {
+    mt = local % m_tiles;
+    const int rest = local / m_tiles;
+    tt = rest % tiles;
+    ks = rest / tiles;
+  } else if (tiles <= 4) {  // few token tiles: a weight block's tiles back to back
+    mt = local / tiles;
+    tt = local - mt * tiles;
+  } else {  // many token tiles: all weight blocks of a token tile back to back
+    mt = local % m_tiles;
+    tt = local / m_tiles;
+  }
+  Unit r;
+  r.g = lo;
+  r.mt = mt;
+  r.r0 = gstart[lo] + tt * BN;
+  r.nt = min(BN, cnt - tt * BN);
+  r.kb0 = MODE == MODE_ROUTER ? ks * p.kb_per : 0;
+  r.kb1 = MODE == MODE_ROUTER ? min(KB, r.kb0 + p.kb_per) : KB;
+  return r;
+}
+
+// One warp builds the schedule in shared memory.  Batch boundaries are made
+// safe first: each clamped to [0, max_rows] and forced non-decreasing
+// (running max), so every batch lies inside the row buffers whatever the
+// caller passed; any change is flagged.  Then prefix[g] = units before group
+// g, with m_tiles x ceil(rows / BN) (x ksplit for the router) units per group.
+template <int MODE, int BN>
+__device__ __forceinline__ void build_schedule(const Params& p, int m_tiles, int* prefix,
+                                               int* gstart) {
+  const int lane = threadIdx.x & 31;
+  int run = 0;
+  for (int base = 0; base <= p.n_groups; base += 32) {
+    const int i = base + lane;
+    int v = 0, raw = 0;
+    if (i <= p.n_groups) {
+      raw = p.offsets ? p.offsets[i] : (i == 0 ? 0 : p.rows_single);
+      v = min(max(raw, 0), p.max_rows);
+    }
+    int m = max(v, run);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) m = max(m, __shfl_up_sync(0xffffffffu, m, o));
+    if (i <= p.n_groups) {
+      gstart[i] = m;
+      if (m != raw) flag_error(p.err, kErrDeviceInput);
+    }
+    run = __shfl_sync(0xffffffffu, m, 31);
+  }
+  __syncwarp();
+  int carry = 0;
+  if (lane == 0) prefix[0] = 0;
+  for (int base = 0; base < p.n_groups; base += 32) {
+    const int g = base + lane;
+    int units = 0;
+    if (g < p.n_groups) {
+      const int cnt = gstart[g + 1] - gstart[g];
+      units = m_tiles * ((cnt + BN - 1) / BN) * (MODE == MODE_ROUTER ? p.ksplit : 1);
+    }
+    int incl = units;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (g < p.n_groups) prefix[g + 1] = carry + incl;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+}
+
+// Warp-uniform bounded wait: every lane polls, the timeout decision is lane 0's.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, int* err) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    const bool ok = mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    if ((i & 31u) == 31u) {
+      int stop = 0;
+      if ((threadIdx.x & 31) == 0) {
+        if (*abort_flag) {
+          stop = 1;
+        } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          *abort_flag = 1;
+          flag_error(err, kErrTimeout);
+          stop = 1;
+        }
+      }
+      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    }
+  }
+}
+
+// Bounded wait used while winding down: ignores the abort flag.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, int* err) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      flag_error(err, kErrTimeout);
+      return;
+    }
+  }
+}
+
+// Epilogue, run by the kEpiWarps epilogue warps (warp indices first_warp ..
+// first_warp + 7): for every unit of this CTA, wait for its accumulators in
+// TMEM, read them with tcgen05.ld (a warp may only read its lane quarter,
+// warp % 4; the two warps of a quarter take alternate 16-column chunks),
+// apply the mode's epilogue and store, then hand the TMEM buffer back.
+//   MODE_ROUTER : partial logits, fp32
+//   MODE_GATEUP : H = silu(gate) * up, bf16 (fp16 when H_F16; a value beyond
+//                 fp16's range is flagged as an input error)
+//   MODE_DOWN   : y_perm = acc * row_scale, bf16
+template <int MODE, int BN, int NACC, int NBUF, bool H_F16 = false>
+__device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_tiles, int KB,
+                                              const int* prefix, const int* gstart,
+                                              uint32_t tmem_base, uint32_t accf0,
+                                              uint32_t acce0, volatile int* abort_flag,
+                                              int first_warp) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3;                   // TMEM lane quarter this warp may access
+  const int half = (warp - first_warp) / 4;  // alternate 16-column chunks
+  int it = 0;
+  for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+    const Unit t = decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
+    const int buf = NBUF == 2 ? (it & 1) : 0;
+    const uint32_t use = NBUF == 2 ? (uint32_t)(it >> 1) : (uint32_t)it;
+    if (!mbar_wait_warp(accf0 + 8u * buf, use & 1u, abort_flag, p.err)) break;
+    tc_fence_after();
+    const int m = t.mt * 128 + q * 32 + lane;  // weight row within the group
+    const bool mvalid = m < p.Mg;
+    const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NACC * BN);
+    for (int c0 = 16 * half; c0 < t.nt; c0 += 32) {
+      uint32_t a[16], b[16];
+      tmem_ld16(tb + c0, a);
+      if (NACC == 2) tmem_ld16(tb + BN + c0, b);
+      tmem_ld_wait();
+      if (mvalid) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = c0 + j;
+          if (col >= t.nt) break;
+          const size_t row = (size_t)(t.r0 + col);
+          const float v = __uint_as_float(a[j]);
+          if (MODE == MODE_ROUTER) {
+            const size_t chunk = (size_t)(t.kb0 / p.kb_per);
+            static_cast<float*>(p.out)[(chunk * p.rows_single + row) * p.ldo + m] = v;
+          } else if (MODE == MODE_GATEUP) {
+            const float hval = silu_f32(v) * __uint_as_float(b[j]);
+            if (H_F16) {
+              const __half hh = __float2half_rn(hval);
+              if (__hisinf(hh)) flag_error(p.err, kErrDeviceInput);
+              static_cast<__half*>(p.out)[row * p.ldo + m] = hh;
+            } else {
+              static_cast<__nv_bfloat16*>(p.out)[row * p.ldo + m] = __float2bfloat16_rn(hval);
+            }
+          } else {
+            const float sc = p.row_scale ? p.row_scale[row] : 1.f;
+            static_cast<__nv_bfloat16*>(p.out)[row * p.ldo + m] = __float2bfloat16_rn(v * sc);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(acce0 + 8u * buf);
+  }
+}
+
+}  // namespace tc
+
+// Host: 2-D tiled tensor map (row-major [rows, inner] of `elsize`-byte elements),
+// boxes of box_rows x box_inner; swizzle128 selects the 128-byte swizzle the MMA
+// operands use (box_inner * elsize must then be 128).
+bool make_tmap_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType dtype, int elsize,
+                  uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+                  bool swizzle128);
+
+}  // namespace moe

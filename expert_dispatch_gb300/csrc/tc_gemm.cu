@@ -16,15 +16,17 @@
 //     to BN token rows of the expert's batch, so a batch of any size down to
 //     one token costs N = 16 columns instead of a 128-row tile; weights are
 //     streamed exactly once per (expert, 128-row block, token tile).
-//   * Work unit = (expert, 128-row weight block, token tile).  Units of one
-//     weight block are adjacent in the schedule so CTAs running at the same
-//     time share its bytes through L2.
+//   * Work unit = (expert, 128-row weight block, token tile); the order of
+//     units is described at tc::decode_unit.
 //   * Warp 0 lane 0 issues TMA loads (128-byte swizzle) into a STAGES-deep
 //     shared-memory ring; warp 1 lane 0 issues tcgen05.mma (bf16 x bf16 ->
-//     fp32 in TMEM) and commits each stage back to the loader; warps 2-5 read
+//     fp32 in TMEM) and commits each stage back to the loader; warps 2-9 read
 //     the accumulators with tcgen05.ld and apply the epilogue (SwiGLU, row
-//     scale) while the next unit's MMAs run into the other TMEM buffer.
-//   * Token rows are loaded in 32-row boxes, only as many as the unit has.
+//     scale) while, with two TMEM buffers, the next unit's MMAs run.
+//   * Token rows are loaded in 32-row boxes for partial tiles and one
+//     BN-row box for full tiles.
+//   * Launched with programmatic dependent launch: the first unit's weight
+//     tiles are requested before waiting for the previous kernel.
 //   * Every wait is bounded (1 s); on expiry the CTA records a timeout in the
 //     error word, drains its own copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -34,14 +36,17 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int MODE_ROUTER = 0, MODE_GATEUP = 1, MODE_DOWN = 2;
-constexpr int kMaxGroups = 1028;
-constexpr int kEpiWarps = 8;                   // two per TMEM lane quarter
-constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, epilogue
+using tc::MODE_DOWN;
+using tc::MODE_GATEUP;
+using tc::MODE_ROUTER;
+using tc::Params;
+using tc::Unit;
+constexpr int kThreads = 32 * (2 + tc::kEpiWarps);  // producer, MMA, epilogue
 
 template <int MODE, int BN, int STAGES>
 struct Cfg {
@@ -58,105 +63,12 @@ struct Cfg {
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr int PREFIX_OFF = MISC_OFF + 16;
-  static constexpr int GSTART_OFF = PREFIX_OFF + 4 * (kMaxGroups + 1);
-  static constexpr int SMEM_TOTAL = GSTART_OFF + 4 * (kMaxGroups + 1) + 1024;
+  static constexpr int GSTART_OFF = PREFIX_OFF + 4 * (tc::kMaxGroups + 1);
+  static constexpr int SMEM_TOTAL = GSTART_OFF + 4 * (tc::kMaxGroups + 1) + 1024;
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "token tile");
   static_assert(COLS <= 512, "TMEM columns");
   static_assert(SMEM_TOTAL <= 232448, "shared memory");
 };
-
-struct Params {
-  const int32_t* offsets;  // [n_groups + 1] batch boundaries, or null
-  int n_groups;
-  int rows_single;         // rows of the single group when offsets is null
-  int Mg;                  // weight rows per group
-  int K;                   // reduction length (multiple of 64)
-  void* out;
-  int ldo;                 // output row stride, elements
-  const float* row_scale;  // MODE_DOWN: per-row factor or null
-  int* err;
-  int max_rows;            // rows of the token operand / output; batch bounds are clamped to it
-  int ksplit;              // MODE_ROUTER: K is cut into ksplit chunks of kb_per 64-wide blocks,
-  int kb_per;              //   each chunk's partial sums go to out + chunk * rows * ldo
-};
-
-struct Unit {
-  int g, mt, r0, nt, kb0, kb1;
-};
-
-// Unit u -> (group, weight block, token rows, K range).  A group with at most
-// four token tiles is ordered token-tile-minor (a weight block's tiles run
-// back to back, so its bytes come from HBM once); a group with more is
-// ordered weight-block-minor (the CTAs running together cover all weight
-// blocks of a few token tiles, so the expert's weights and those token rows
-// stay in L2 while its tiles are swept).  The router always uses the latter.
-template <int MODE, int BN>
-__device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int* gstart,
-                                            int n_groups, int m_tiles, int KB, const Params& p) {
-  int lo = 0, hi = n_groups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (prefix[mid] <= u) lo = mid; else hi = mid - 1;
-  }
-  const int local = u - prefix[lo];
-  const int cnt = gstart[lo + 1] - gstart[lo];
-  const int tiles = (cnt + BN - 1) / BN;
-  int mt, tt, ks = 0;
-  if (MODE == MODE_ROUTER) {
-    mt = local % m_tiles;
-    const int rest = local / m_tiles;
-    tt = rest % tiles;
-    ks = rest / tiles;
-  } else if (tiles <= 4) {  // few token tiles: a weight block's tiles back to back
-    mt = local / tiles;
-    tt = local - mt * tiles;
-  } else {  // many token tiles: all weight blocks of a token tile back to back
-    mt = local % m_tiles;
-    tt = local / m_tiles;
-  }
-  Unit r;
-  r.g = lo;
-  r.mt = mt;
-  r.r0 = gstart[lo] + tt * BN;
-  r.nt = min(BN, cnt - tt * BN);
-  r.kb0 = MODE == MODE_ROUTER ? ks * p.kb_per : 0;
-  r.kb1 = MODE == MODE_ROUTER ? min(KB, r.kb0 + p.kb_per) : KB;
-  return r;
-}
-
-// Warp-uniform bounded wait: every lane polls, the timeout decision is lane 0's.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
-                                               volatile int* abort_flag, int* err) {
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t i = 0;; ++i) {
-    const bool ok = mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, ok)) return true;
-    if ((i & 31u) == 31u) {
-      int stop = 0;
-      if ((threadIdx.x & 31) == 0) {
-        if (*abort_flag) {
-          stop = 1;
-        } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          *abort_flag = 1;
-          flag_error(err, kErrTimeout);
-          stop = 1;
-        }
-      }
-      if (__shfl_sync(0xffffffffu, stop, 0)) return false;
-    }
-  }
-}
-
-// Bounded wait used while winding down: ignores the abort flag.
-__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, int* err) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      flag_error(err, kErrTimeout);
-      return;
-    }
-  }
-}
 
 template <int MODE, int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -172,8 +84,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar0 = sbase + C::BAR_OFF;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-  auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + C::NBUF + b); };
+  const uint32_t accf0 = bar0 + 8u * (2 * STAGES);
+  const uint32_t acce0 = bar0 + 8u * (2 * STAGES + C::NBUF);
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 2 * C::NBUF);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
@@ -190,8 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < C::NBUF; ++b) {
-      mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), kEpiWarps);
+      mbar_init(accf0 + 8u * b, 1);
+      mbar_init(acce0 + 8u * b, tc::kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -205,48 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
-  if (warp == 2) {
-    // Batch boundaries, made safe: each clamped to [0, max_rows] and forced
-    // non-decreasing (running max), so every batch lies inside the row
-    // buffers whatever the caller passed; any change is flagged.
-    int run = 0;
-    for (int base = 0; base <= p.n_groups; base += 32) {
-      const int i = base + lane;
-      int v = 0, raw = 0;
-      if (i <= p.n_groups) {
-        raw = p.offsets ? p.offsets[i] : (i == 0 ? 0 : p.rows_single);
-        v = min(max(raw, 0), p.max_rows);
-      }
-      int m = max(v, run);
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) m = max(m, __shfl_up_sync(0xffffffffu, m, o));
-      if (i <= p.n_groups) {
-        gstart[i] = m;
-        if (m != raw) flag_error(p.err, kErrDeviceInput);
-      }
-      run = __shfl_sync(0xffffffffu, m, 31);
-    }
-    __syncwarp();
-    // units per group: m_tiles x ceil(rows / BN); prefix over groups
-    int carry = 0;
-    if (lane == 0) prefix[0] = 0;
-    for (int base = 0; base < p.n_groups; base += 32) {
-      const int g = base + lane;
-      int units = 0;
-      if (g < p.n_groups) {
-        const int cnt = gstart[g + 1] - gstart[g];
-        units = m_tiles * ((cnt + BN - 1) / BN) * (MODE == MODE_ROUTER ? p.ksplit : 1);
-      }
-      int incl = units;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (g < p.n_groups) prefix[g + 1] = carry + incl;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
+  if (warp == 2) tc::build_schedule<MODE, BN>(p, m_tiles, prefix, gstart);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -264,7 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // output (the token rows) is loaded only after the wait.
       int n_pre = 0;
       if ((int)blockIdx.x < total) {
-        const Unit t = decode_unit<MODE, BN>(blockIdx.x, prefix, gstart, p.n_groups, m_tiles, KB, p);
+        const Unit t =
+            tc::decode_unit<MODE, BN>(blockIdx.x, prefix, gstart, p.n_groups, m_tiles, KB, p);
         const uint32_t bytes = C::NA * C::A_BYTES + ((t.nt + 31) / 32) * 4096;
         const int arow = t.g * p.Mg + t.mt * 128;
         n_pre = min(STAGES, t.kb1 - t.kb0);
@@ -280,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool first = true;
       for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x) {
         if (u + (int)gridDim.x >= total) pdl_trigger();  // this CTA's last unit
-        const Unit t = decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
+        const Unit t = tc::decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
         const int nchunks = (t.nt + 31) / 32;
         const uint32_t bytes = C::NA * C::A_BYTES + nchunks * 4096;
         const int arow = t.g * p.Mg + t.mt * 128;
@@ -318,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((int)blockIdx.x >= total) pdl_trigger();
       // wind down: every copy this thread started has landed before exit
       for (int s = 0; s < STAGES; ++s)
-        if (armed & (1u << s)) mbar_wait_drain(full_bar(s), (armed_parity >> s) & 1u, p.err);
+        if (armed & (1u << s)) tc::mbar_wait_drain(full_bar(s), (armed_parity >> s) & 1u, p.err);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -327,12 +199,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool issued = false;
       for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x, ++it) {
-        const Unit t = decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
+        const Unit t = tc::decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
         const int n_mma = max(16, (t.nt + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(128, n_mma);
         const int buf = C::NBUF == 2 ? (it & 1) : 0;
         const uint32_t use = C::NBUF == 2 ? (uint32_t)(it >> 1) : (uint32_t)it;
-        if (!mbar_wait(acce_bar(buf), (use & 1u) ^ 1u, abort_flag, p.err)) break;
+        if (!mbar_wait(acce0 + 8u * buf, (use & 1u) ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + (uint32_t)(buf * C::NACC * BN);
         bool ok = true;
@@ -360,57 +232,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(accf_bar(buf));
+        umma_commit(accf0 + 8u * buf);
       }
       // wind down: every MMA this thread issued has completed before TMEM is freed
       if (issued) {
         umma_commit(drain_bar);
-        mbar_wait_drain(drain_bar, 0, p.err);
+        tc::mbar_wait_drain(drain_bar, 0, p.err);
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..9)
-    const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int half = (warp - 2) / 4;  // the two warps of a quarter take alternate 16-column chunks
-    int it = 0;
-    for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-      const Unit t = decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
-      const int buf = C::NBUF == 2 ? (it & 1) : 0;
-      const uint32_t use = C::NBUF == 2 ? (uint32_t)(it >> 1) : (uint32_t)it;
-      if (!mbar_wait_warp(accf_bar(buf), use & 1u, abort_flag, p.err)) break;
-      tc_fence_after();
-      const int m = t.mt * 128 + q * 32 + lane;  // weight row within the group
-      const bool mvalid = m < p.Mg;
-      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * C::NACC * BN);
-      for (int c0 = 16 * half; c0 < t.nt; c0 += 32) {
-        uint32_t a[16], b[16];
-        tmem_ld16(tb + c0, a);
-        if (C::NA == 2) tmem_ld16(tb + BN + c0, b);
-        tmem_ld_wait();
-        if (mvalid) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = c0 + j;
-            if (col >= t.nt) break;
-            const size_t row = (size_t)(t.r0 + col);
-            const float v = __uint_as_float(a[j]);
-            if (MODE == MODE_ROUTER) {
-              const size_t chunk = (size_t)(t.kb0 / p.kb_per);
-              static_cast<float*>(p.out)[(chunk * p.rows_single + row) * p.ldo + m] = v;
-            } else if (MODE == MODE_GATEUP) {
-              const float hval = silu_f32(v) * __uint_as_float(b[j]);
-              static_cast<__nv_bfloat16*>(p.out)[row * p.ldo + m] = __float2bfloat16_rn(hval);
-            } else {
-              const float sc = p.row_scale ? p.row_scale[row] : 1.f;
-              static_cast<__nv_bfloat16*>(p.out)[row * p.ldo + m] = __float2bfloat16_rn(v * sc);
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(buf));
-    }
+    tc::epilogue_loop<MODE, BN, C::NACC, C::NBUF>(p, total, m_tiles, KB, prefix, gstart,
+                                                  tmem_base, accf0, acce0, abort_flag, 2);
   }
 
   tc_fence_before();
@@ -445,15 +278,8 @@ EncodeTiledFn encode_fn() {
 // bf16 matrix [rows, inner] (row-major), boxes of box_rows x 64, 128-byte swizzle
 bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
                uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tmap_2d(tm, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, rows, 64, box_rows,
+                      true);
 }
 
 template <int MODE, int BN, int STAGES>
@@ -479,6 +305,21 @@ cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtens
 }
 
 }  // namespace
+
+bool make_tmap_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType dtype, int elsize,
+                  uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
+                  bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * (uint64_t)elsize};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(tm, dtype, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // Rows of the workspace's permuted-row buffers: P rounded up so that every
 // 32-row box a unit may touch lies inside the buffer.

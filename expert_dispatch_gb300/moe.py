@@ -37,7 +37,8 @@ MOE_BF16 = 1
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status",
             "moe_status_string", "moe_launch_count", "moe_profile_enable", "moe_profile_query",
-            "moe_expert_ffn_noalloc", "moe_combine_partial")
+            "moe_expert_ffn_noalloc", "moe_combine_partial", "moe_quantize_q8_0",
+            "moe_expert_ffn_q8", "moe_layer_forward_q8")
 
 
 class MoeError(RuntimeError):
@@ -52,6 +53,11 @@ class LayerDesc(ctypes.Structure):
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("I", ctypes.c_int32),
                 ("S", ctypes.c_int32), ("gate", ctypes.c_int32), ("norm_topk", ctypes.c_int32),
                 ("routed_scaling", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class Q8WeightStruct(ctypes.Structure):
+    """moe_q8_weight"""
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
 
 
 def make_desc(T, d, E, k, I, S=0, gate=MOE_GATE_SOFTMAX_TOPK, norm_topk=0, routed_scaling=1.0,
@@ -94,6 +100,10 @@ def lib():
     L.moe_launch_count.restype = ctypes.c_int64
     L.moe_expert_ffn_noalloc.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_combine_partial.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    Q = ctypes.POINTER(Q8WeightStruct)
+    L.moe_quantize_q8_0.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
+    L.moe_expert_ffn_q8.argtypes = [D, vp, vp, vp, vp, Q, Q, Q, vp, vp, sz, vp]
+    L.moe_layer_forward_q8.argtypes = [D, vp, vp, vp, vp, Q, Q, Q, vp, vp, vp, vp, vp, sz, vp]
     L.moe_profile_enable.argtypes = [i32]
     L.moe_profile_query.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
                                     ctypes.POINTER(ctypes.c_float)]
@@ -290,6 +300,88 @@ def moe_layer_forward(desc, x, Wr, logit_bias, sel_bias, Wg, Wu, Wd, residual, y
     _check(st, "moe_layer_forward")
 
 
+# ---------------------------------------------------------------- Q8_0 expert weights
+class Q8Weight:
+    """A Q8_0 projection on the device: int8 codes [n, rows, K] and the f16 scale
+    bit patterns (held as int16) [n, K/32, rows]."""
+
+    def __init__(self, q: torch.Tensor, scale: torch.Tensor):
+        if q.dtype != torch.int8 or scale.dtype != torch.int16:
+            raise TypeError("Q8_0 codes must be int8 and scales int16 (f16 bits)")
+        n, rows, K = q.shape
+        if tuple(scale.shape) != (n, K // 32, rows):
+            raise ValueError("scale shape %s, expected %s" % (tuple(scale.shape), (n, K // 32, rows)))
+        self.q, self.scale = q, scale
+
+    def struct(self):
+        return Q8WeightStruct(_p(self.q, torch.int8, "q"), _p(self.scale, torch.int16, "scale"))
+
+    @property
+    def shape(self):
+        return tuple(self.q.shape)
+
+
+def moe_quantize_q8_0(w, q, scale, stream=None):
+    """Q8_0 codes and scales of w [n, rows, K] (fp32 or bf16, on the device)."""
+    n, rows, K = w.shape
+    dt = {torch.float32: MOE_F32, torch.bfloat16: MOE_BF16}.get(w.dtype)
+    if dt is None:
+        raise TypeError("w must be fp32 or bf16")
+    _need(q, (n, rows, K), "q")
+    _need(scale, (n, K // 32, rows), "scale")
+    st = lib().moe_quantize_q8_0(n, rows, K, dt, _p(w, w.dtype, "w"), _p(q, torch.int8, "q"),
+                                 _p(scale, torch.int16, "scale"), _stream(stream))
+    _check(st, "moe_quantize_q8_0")
+
+
+def quantize_q8_0(w, stream=None) -> Q8Weight:
+    n, rows, K = w.shape
+    q = torch.empty((n, rows, K), dtype=torch.int8, device=w.device)
+    s = torch.empty((n, K // 32, rows), dtype=torch.int16, device=w.device)
+    moe_quantize_q8_0(w, q, s, stream)
+    return Q8Weight(q, s)
+
+
+def _q8_check(desc, Wg, Wu, Wd):
+    nE = desc.E + desc.S
+    for name, W, shape in (("Wg", Wg, (nE, desc.I, desc.d)), ("Wu", Wu, (nE, desc.I, desc.d)),
+                           ("Wd", Wd, (nE, desc.d, desc.I))):
+        if not isinstance(W, Q8Weight) or W.shape != shape:
+            raise ValueError("%s must be a Q8Weight of shape %s" % (name, shape))
+
+
+def moe_expert_ffn_q8(desc, x, expert_offsets, token_indices, slot_w, Wg, Wu, Wd, y_perm, ws,
+                      stream=None):
+    _q8_check(desc, Wg, Wu, Wd)
+    _need(x, (desc.T, desc.d), "x")
+    _need(y_perm, (desc.T * (desc.k + desc.S), desc.d), "y_perm")
+    g, u, d = Wg.struct(), Wu.struct(), Wd.struct()
+    st = lib().moe_expert_ffn_q8(
+        ctypes.byref(desc), _p(x, torch.bfloat16, "x"),
+        _p(expert_offsets, torch.int32, "expert_offsets"),
+        _p(token_indices, torch.int32, "token_indices"), _p(slot_w, torch.float32, "slot_w"),
+        ctypes.byref(g), ctypes.byref(u), ctypes.byref(d), _p(y_perm, torch.bfloat16, "y_perm"),
+        _p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream))
+    _check(st, "moe_expert_ffn_q8")
+
+
+def moe_layer_forward_q8(desc, x, Wr, logit_bias, sel_bias, Wg, Wu, Wd, residual, y,
+                         topk_ids_out, topk_w_out, ws, stream=None):
+    _q8_check(desc, Wg, Wu, Wd)
+    _need(x, (desc.T, desc.d), "x")
+    _need(Wr, (desc.E, desc.d), "Wr")
+    _need(y, (desc.T, desc.d), "y")
+    g, u, d = Wg.struct(), Wu.struct(), Wd.struct()
+    st = lib().moe_layer_forward_q8(
+        ctypes.byref(desc), _p(x, torch.bfloat16, "x"), _p(Wr, torch.bfloat16, "Wr"),
+        _p(logit_bias, torch.float32, "logit_bias"), _p(sel_bias, torch.float32, "sel_bias"),
+        ctypes.byref(g), ctypes.byref(u), ctypes.byref(d),
+        _p(residual, torch.float32, "residual"), _p(y, torch.float32, "y"),
+        _p(topk_ids_out, torch.int32, "topk_ids_out"), _p(topk_w_out, torch.float32, "topk_w_out"),
+        _p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream))
+    _check(st, "moe_layer_forward_q8")
+
+
 def moe_get_device_status(ws, clear=False, stream=None) -> int:
     """Synchronizes the stream and returns the workspace's sticky device status."""
     return lib().moe_get_device_status(_p(ws, torch.uint8, "workspace"), ws.numel(),
@@ -319,8 +411,10 @@ class MoeLayer:
     moe_layer_forward.  Weights are used in place (no copies)."""
 
     def __init__(self, desc: LayerDesc, Wr, Wg, Wu, Wd, logit_bias=None, sel_bias=None):
+        """Wg/Wu/Wd are bf16/fp32 tensors, or Q8Weight (Q8_0 experts, bf16 layers)."""
         self.desc = desc
         self.Wr, self.Wg, self.Wu, self.Wd = Wr, Wg, Wu, Wd
+        self.q8 = isinstance(Wg, Q8Weight)
         self.logit_bias, self.sel_bias = logit_bias, sel_bias
         self.ws = alloc_workspace(desc, device=Wr.device)
 
@@ -328,8 +422,9 @@ class MoeLayer:
         d = self.desc
         if y is None:
             y = torch.empty((d.T, d.d), dtype=torch.float32, device=x.device)
-        moe_layer_forward(d, x, self.Wr, self.logit_bias, self.sel_bias, self.Wg, self.Wu,
-                          self.Wd, residual, y, topk_ids, topk_w, self.ws, stream)
+        fwd = moe_layer_forward_q8 if self.q8 else moe_layer_forward
+        fwd(d, x, self.Wr, self.logit_bias, self.sel_bias, self.Wg, self.Wu, self.Wd, residual, y,
+            topk_ids, topk_w, self.ws, stream)
         return y
 
     def forward_host(self, x_host, y_host, x_dev, y_dev, stream=None):

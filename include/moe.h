@@ -219,6 +219,44 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
                              int32_t* topk_ids_out, float* topk_w_out, void* workspace,
                              size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- Q8_0 expert weights
+   ("Distributed MoE", quantization table: Q8_0 = 32-element blocks with one
+   f16 scale, about 8.5 bits per weight; the prepare job block-quantizes
+   each expert projection, and a holder decodes it with its dequant path.)
+   The block contents are GGUF's; the arrangement is planar for the GPU:
+     q     int8 codes in the weight's own layout, [n_mats, rows, K]
+     scale f16 bit patterns, transposed per matrix, [n_mats, K/32, rows]
+   Block b of row r represents scale[m][b][r] * q[m][r][32b .. 32b+31]. */
+typedef struct {
+  const void* q;      /* int8  [E+S, rows, K] */
+  const void* scale;  /* f16   [E+S, K/32, rows] */
+} moe_q8_weight;
+
+/* moe_quantize_q8_0 -- quantize n_mats row-major [rows, K] matrices (fp32 or
+   bf16, src_dtype a moe_dtype) into Q8_0: for each 32-element block,
+   d = max|w| / 127, q = round-half-away(w / d) computed as w * (1/d) in fp32,
+   scale = f16(d).  K % 32 == 0.  q and scale are device outputs sized as in
+   moe_q8_weight. */
+moe_status moe_quantize_q8_0(int n_mats, int rows, int K, int src_dtype, const void* w, void* q,
+                             void* scale, void* stream);
+
+/* moe_expert_ffn_q8 / moe_layer_forward_q8 -- moe_expert_ffn and
+   moe_layer_forward with Q8_0 expert projections (router weights stay in the
+   layer's dtype).  desc->dtype must be MOE_BF16 (activations); each weight
+   is dequantized on chip (scale * q rounded to bf16) and fed to the same
+   tensor-core path.  Wg/Wu have rows = I and K = d; Wd has rows = d, K = I. */
+moe_status moe_expert_ffn_q8(const moe_layer_desc* desc, const void* x,
+                             const int32_t* expert_offsets, const int32_t* token_indices,
+                             const float* slot_w, const moe_q8_weight* Wg,
+                             const moe_q8_weight* Wu, const moe_q8_weight* Wd, void* y_perm,
+                             void* workspace, size_t ws_bytes, void* stream);
+moe_status moe_layer_forward_q8(const moe_layer_desc* desc, const void* x, const void* Wr,
+                                const float* logit_bias, const float* sel_bias,
+                                const moe_q8_weight* Wg, const moe_q8_weight* Wu,
+                                const moe_q8_weight* Wd, const float* residual, float* y,
+                                int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                                size_t ws_bytes, void* stream);
+
 /* Synchronizes `stream`, then reports the sticky device flag held in the
    workspace: MOE_OK, MOE_ERR_DEVICE_INPUT or MOE_ERR_TIMEOUT (MOE_ERR_CUDA if
    the copy itself fails).  clear != 0 resets the flag afterwards.          */

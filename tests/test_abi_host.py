@@ -24,7 +24,7 @@ def L():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_five_layer_calls():
@@ -37,7 +37,7 @@ def test_header_declares_the_five_layer_calls():
 def test_library_exports_every_declared_symbol(L):
     out = subprocess.run(["nm", "-D", "--defined-only", moe.LIB_PATH], capture_output=True,
                          text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (moe_[a-z_]+)$", out, flags=re.M))
+    exported = set(re.findall(r"\bT (moe_[a-z0-9_]+)$", out, flags=re.M))
     missing = [f for f in declared_functions() if f not in exported]
     assert not missing, missing
     assert set(moe.EXPORTED) == set(declared_functions())

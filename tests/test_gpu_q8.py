@@ -1,0 +1,115 @@
+"""Q8_0 expert weights on the GPU against the fp64 oracle.
+
+The quantizer's integer codes and f16 scales must match the oracle's bit for
+bit (both decide in fp32).  The FFN and the layer forward on Q8_0 weights are
+compared with the oracle run on its own dequantization of the same bf16
+weights (exact scale * q in fp64); the GPU rounds each dequantized weight to
+bf16 before the tensor cores, which the 1e-2 output tolerance covers.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from expert_dispatch_gb300 import moe
+from expert_dispatch_gb300.inputs import CONFIGS, KIMI_DECODE, LayerConfig, make_inputs
+from tests.helpers import enforce_margins, host, rel_err
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from expert_dispatch_gb300 import build
+    build.build()
+
+
+def _oracle_deq(W):
+    """Host copy of W [n, R, K] -> the oracle's Q8_0 codes -> exact fp64 weights."""
+    q, s = oracle.quantize_q8_0(host(W))
+    return oracle.dequantize_q8_0(q, s)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_quantize_matches_oracle_bit_for_bit(dtype):
+    g = torch.Generator(device=DEV).manual_seed(17)
+    w = (torch.randn((5, 192, 256), generator=g, device=DEV) * 0.03).to(dtype)
+    w[1, 3, 64:96] = 0                      # an all-zero block
+    w[2, 7, :32] *= 1000                    # a large block
+    w[4, :, 128:160] = -w[4, :, 128:160].abs()
+    qw = moe.quantize_q8_0(w)
+    q_ref, s_ref = oracle.quantize_q8_0(host(w))
+    np.testing.assert_array_equal(host(qw.q).numpy(), q_ref)
+    np.testing.assert_array_equal(host(qw.scale).numpy().view(np.uint16), s_ref)
+
+
+Q8_CASES = [
+    LayerConfig("q_small_tiles", T=67, d=128, E=8, I=192, k=2, S=1, gate=1, norm_topk=1,
+                routed_scaling=2.5, sel_bias_range=0.1),
+    LayerConfig("q_mid_tiles", T=300, d=192, E=8, I=320, k=2, S=1, gate=1, norm_topk=1,
+                routed_scaling=2.5, sel_bias_range=0.1),
+    LayerConfig("q_large_tiles", T=600, d=256, E=4, I=320, k=2),
+    LayerConfig("q_hot_expert", T=2000, d=128, E=8, I=128, k=2, zipf_s=1.2),
+    LayerConfig("q_one_token", T=1, d=512, E=32, I=256, k=4, S=1, gate=1, norm_topk=1,
+                routed_scaling=2.8, sel_bias_range=0.1),
+]
+
+
+@pytest.mark.parametrize("cfg", Q8_CASES, ids=lambda c: c.name)
+def test_expert_ffn_q8_parity(cfg):
+    inp = enforce_margins(make_inputs(cfg, seed=23, device=DEV), cfg, 23)
+    ids, _ = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
+                          norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling,
+                          logit_bias=host(inp["logit_bias"]), sel_bias=host(inp["sel_bias"]))
+    plan = oracle.plan(ids, cfg.E, cfg.S)
+    desc = moe.desc_from_config(cfg)
+    ws = moe.alloc_workspace(desc)
+    P = cfg.T * (cfg.k + cfg.S)
+    Wg, Wu, Wd = (moe.quantize_q8_0(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    y_perm = torch.zeros((P, cfg.d), dtype=torch.bfloat16, device=DEV)
+    moe.moe_expert_ffn_q8(desc, inp["x"], torch.from_numpy(plan["expert_offsets"]).to(DEV),
+                          torch.from_numpy(plan["token_indices"]).to(DEV), None, Wg, Wu, Wd,
+                          y_perm, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    dg, du, dd = (_oracle_deq(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    o, tok = plan["expert_offsets"], plan["token_indices"]
+    ref = np.zeros((P, cfg.d))
+    for e in range(cfg.E + cfg.S):
+        if o[e + 1] > o[e]:
+            ref[o[e]:o[e + 1]] = oracle.expert_rows(host(inp["x"]), dg[e], du[e], dd[e],
+                                                    tok[o[e]:o[e + 1]])
+    got = host(y_perm).double().numpy()
+    assert rel_err(got, ref) <= 1e-2, rel_err(got, ref)
+
+
+@pytest.mark.parametrize("cfg,n_sample", [(KIMI_DECODE.with_T(1), 1), (KIMI_DECODE.with_T(64), 6),
+                                          (CONFIGS["qwen_t512"], 24)],
+                         ids=["kimi_decode_T1", "kimi_decode_T64", "qwen_t512"])
+def test_layer_forward_q8_full_size(cfg, n_sample):
+    inp = enforce_margins(make_inputs(cfg, seed=0, device=DEV), cfg, 0)
+    desc = moe.desc_from_config(cfg)
+    Wg, Wu, Wd = (moe.quantize_q8_0(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    layer = moe.MoeLayer(desc, inp["Wr"], Wg, Wu, Wd, logit_bias=inp["logit_bias"],
+                         sel_bias=inp["sel_bias"])
+    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    y = layer.forward(inp["x"], topk_ids=ids)
+    assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
+    kw = dict(norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling,
+              logit_bias=host(inp["logit_bias"]), sel_bias=host(inp["sel_bias"]))
+    ids_ref, _ = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate, **kw)
+    np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
+    rng = np.random.default_rng(1)
+    tokens = np.sort(rng.choice(cfg.T, size=n_sample, replace=False)).astype(np.int32)
+    needed = set(np.unique(ids_ref[tokens]).tolist()) | set(range(cfg.E, cfg.E + cfg.S))
+    nE = cfg.E + cfg.S
+    lists = [[None] * nE for _ in range(3)]
+    for e in sorted(needed):
+        for li, name in enumerate(("Wg", "Wu", "Wd")):
+            lists[li][e] = _oracle_deq(inp[name][e:e + 1])[0]
+    y_ref, _, _ = oracle.forward(host(inp["x"]), oracle.widen(host(inp["Wr"])), *lists, cfg.k,
+                                 cfg.gate, S=cfg.S, tokens=tokens, **kw)
+    got = host(y[torch.from_numpy(tokens).long().to(DEV)]).double().numpy()
+    assert rel_err(got, y_ref) <= 1e-2, rel_err(got, y_ref)
