@@ -126,6 +126,7 @@ __device__ __forceinline__ void build_schedule(const Params& p, int m_tiles, int
 // Warp-uniform bounded wait: every lane polls, the timeout decision is lane 0's.
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
                                                volatile int* abort_flag, int* err) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;  // the common case
   const unsigned long long t0 = globaltimer_ns();
   for (uint32_t i = 0;; ++i) {
     const bool ok = mbar_try_wait(bar, parity);

@@ -303,17 +303,22 @@ __global__ void __launch_bounds__(kThreadsQ8, 1)
           ok = false;
           break;
         }
-        const uint8_t* raw = smem + rs * C::RAW_BYTES;
-        uint8_t* conv = smem + C::CONV_OFF + cs * C::CONV_BYTES;
+        const uint8_t* __restrict__ raw = smem + rs * C::RAW_BYTES;
+        uint8_t* __restrict__ conv = smem + C::CONV_OFF + cs * C::CONV_BYTES;
+        // all loads first (independent, so their latencies overlap), then decode and store
+        uint2 codes[C::CHUNKS_PER_THREAD];
+        __half sh[C::CHUNKS_PER_THREAD];
 #pragma unroll
         for (int i = 0; i < C::CHUNKS_PER_THREAD; ++i) {
           const int op = i >> 2, rr = 32 * (i & 3);  // operand, row offset
-          const uint2 codes = *reinterpret_cast<const uint2*>(raw + code_off + op * C::QA_BYTES +
-                                                              rr * 64);
-          const __half sh =
-              *reinterpret_cast<const __half*>(raw + scale_off + op * C::SA_BYTES + rr * 2);
+          codes[i] = *reinterpret_cast<const uint2*>(raw + code_off + op * C::QA_BYTES + rr * 64);
+          sh[i] = *reinterpret_cast<const __half*>(raw + scale_off + op * C::SA_BYTES + rr * 2);
+        }
+#pragma unroll
+        for (int i = 0; i < C::CHUNKS_PER_THREAD; ++i) {
+          const int op = i >> 2, rr = 32 * (i & 3);
           *reinterpret_cast<uint4*>(conv + dst_off + op * C::CA_BYTES + rr * 128) =
-              dequant8_f16(codes, __halves2half2(sh, sh));
+              dequant8_f16(codes[i], __halves2half2(sh[i], sh[i]));
         }
         fence_async_shared();
         __syncwarp();
