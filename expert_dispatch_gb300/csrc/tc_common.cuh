@@ -163,11 +163,14 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, i
 // TMEM, read them with tcgen05.ld (a warp may only read its lane quarter,
 // warp % 4; the two warps of a quarter take alternate 16-column chunks),
 // apply the mode's epilogue and store, then hand the TMEM buffer back.
+// With NPART = 2 the unit's K blocks were accumulated into two partial sets
+// (even and odd K blocks of the unit, NACC * BN columns apart), added here
+// in that order; a unit with a single K block has only the first.
 //   MODE_ROUTER : partial logits, fp32
 //   MODE_GATEUP : H = silu(gate) * up, bf16 (fp16 when H_F16; a value beyond
 //                 fp16's range is flagged as an input error)
 //   MODE_DOWN   : y_perm = acc * row_scale, bf16
-template <int MODE, int BN, int NACC, int NBUF, bool H_F16 = false>
+template <int MODE, int BN, int NACC, int NBUF, bool H_F16 = false, int NPART = 1>
 __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_tiles, int KB,
                                               const int* prefix, const int* gstart,
                                               uint32_t tmem_base, uint32_t accf0,
@@ -185,11 +188,24 @@ __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_
     tc_fence_after();
     const int m = t.mt * 128 + q * 32 + lane;  // weight row within the group
     const bool mvalid = m < p.Mg;
-    const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NACC * BN);
+    const uint32_t tb =
+        tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NPART * NACC * BN);
+    const bool two = NPART == 2 && t.kb1 - t.kb0 >= 2;
     for (int c0 = 16 * half; c0 < t.nt; c0 += 32) {
       uint32_t a[16], b[16];
       tmem_ld16(tb + c0, a);
       if (NACC == 2) tmem_ld16(tb + BN + c0, b);
+      if (two) {
+        uint32_t a2[16], b2[16];
+        tmem_ld16(tb + NACC * BN + c0, a2);
+        if (NACC == 2) tmem_ld16(tb + NACC * BN + BN + c0, b2);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          a[j] = __float_as_uint(__uint_as_float(a[j]) + __uint_as_float(a2[j]));
+          if (NACC == 2) b[j] = __float_as_uint(__uint_as_float(b[j]) + __uint_as_float(b2[j]));
+        }
+      }
       tmem_ld_wait();
       if (mvalid) {
 #pragma unroll
@@ -226,10 +242,10 @@ __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_
 }  // namespace tc
 
 // Host: 2-D tiled tensor map (row-major [rows, inner] of `elsize`-byte elements),
-// boxes of box_rows x box_inner; swizzle128 selects the 128-byte swizzle the MMA
-// operands use (box_inner * elsize must then be 128).
+// boxes of box_rows x box_inner, with the given shared-memory swizzle (the MMA
+// operands use 128-byte swizzle with 128-byte box rows).
 bool make_tmap_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType dtype, int elsize,
                   uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
-                  bool swizzle128);
+                  CUtensorMapSwizzle swizzle);
 
 }  // namespace moe

@@ -279,7 +279,7 @@ EncodeTiledFn encode_fn() {
 bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
                uint32_t box_rows) {
   return make_tmap_2d(tm, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, rows, 64, box_rows,
-                      true);
+                      CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 template <int MODE, int BN, int STAGES>
@@ -308,7 +308,7 @@ cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtens
 
 bool make_tmap_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType dtype, int elsize,
                   uint64_t inner, uint64_t rows, uint32_t box_inner, uint32_t box_rows,
-                  bool swizzle128) {
+                  CUtensorMapSwizzle swizzle) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, rows};
@@ -316,9 +316,8 @@ bool make_tmap_2d(CUtensorMap* tm, const void* base, CUtensorMapDataType dtype, 
   cuuint32_t box[2] = {box_inner, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(tm, dtype, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Rows of the workspace's permuted-row buffers: P rounded up so that every
