@@ -164,6 +164,18 @@ def kernel_bytes(cfg, kernel, n_active_all):
     return None
 
 
+def kernel_source_sha(kernel):
+    """Hash of the CUDA sources a grouped-GEMM kernel is built from."""
+    csrc = os.path.join(ROOT, "expert_dispatch_gb300", "csrc")
+    files = ["common.cuh", "tc_common.cuh",
+             "tc_gemm_q8.cu" if kernel.endswith("_q8") else "tc_gemm.cu"]
+    h = hashlib.sha256()
+    for name in files:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_record(kernel, cfg):
     """dram bytes per launch from a committed ncu summary, if it was taken on the
     current kernel source and this workload; else None."""
@@ -172,8 +184,7 @@ def traffic_record(kernel, cfg):
         return None
     with open(path) as f:
         recs = json.load(f)
-    src = os.path.join(ROOT, "expert_dispatch_gb300", "csrc", "tc_gemm.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    sha = kernel_source_sha(kernel)
     for r in recs:
         if r.get("kernel") == kernel and r.get("workload") == cfg.name and r.get("source") == sha:
             return r.get("bytes_per_launch")
