@@ -40,8 +40,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 PUBLISHED_CONTEXT = ("53k tok/s per worker at batch 512 on ROCm hardware, expert shape and "
                      "precision unstated (context only, not the same workload)")
 KERNELS = ("router_logits_splitk", "router_logits_tc", "router_topk", "plan_small", "plan_mark",
-           "plan_scan", "plan_place", "gather_rows", "ffn_gateup_simt", "ffn_down_simt", "ffn_gateup_tc",
-           "ffn_down_tc", "ffn_gateup_tc_q8", "ffn_down_tc_q8", "combine")
+           "plan_scan", "plan_place", "gather_rows", "scatter_rows", "ffn_gateup_simt",
+           "ffn_down_simt", "ffn_gateup_tc", "ffn_down_tc", "ffn_gateup_tc_q8", "ffn_down_tc_q8",
+           "combine")
 
 
 def workload(name, T=None, E=None):

@@ -129,13 +129,29 @@ moe_status do_route(const moe_layer_desc* D, const void* x, const void* Wr,
                                         s));
 }
 
-moe_status do_ffn(const moe_layer_desc* D, const void* x, const int32_t* offsets,
-                  const int32_t* tok_idx, const float* slot_w, const void* Wg, const void* Wu,
-                  const void* Wd, void* y_perm, const Ws& W, cudaStream_t s) {
+// Batch rows are permuted into x_perm from the token side when the plan's
+// slot_row map is at hand (the layer call), else from the row side.
+cudaError_t permute_rows(const moe_layer_desc* D, bool to_f16, const void* x,
+                         const int32_t* offsets, const int32_t* tok_idx, const int32_t* slot_row,
+                         const Ws& W, cudaStream_t s) {
   const int P = D->T * (D->k + D->S);
   const int nE = D->E + D->S;
-  cudaError_t e =
-      launch_gather_rows(D->dtype, x, tok_idx, offsets + nE, P, D->T, D->d, W.x_perm, W.flags, s);
+  if (slot_row)
+    return launch_scatter_rows(D->dtype, to_f16, x, slot_row, offsets + nE, D->T, D->k + D->S,
+                               D->d, W.x_perm, W.flags, s);
+  return to_f16 ? launch_gather_rows_to_f16(x, tok_idx, offsets + nE, P, D->T, D->d, W.x_perm,
+                                            W.flags, s)
+                : launch_gather_rows(D->dtype, x, tok_idx, offsets + nE, P, D->T, D->d,
+                                     W.x_perm, W.flags, s);
+}
+
+moe_status do_ffn(const moe_layer_desc* D, const void* x, const int32_t* offsets,
+                  const int32_t* tok_idx, const int32_t* slot_row, const float* slot_w,
+                  const void* Wg, const void* Wu, const void* Wd, void* y_perm, const Ws& W,
+                  cudaStream_t s) {
+  const int P = D->T * (D->k + D->S);
+  const int nE = D->E + D->S;
+  cudaError_t e = permute_rows(D, false, x, offsets, tok_idx, slot_row, W, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (D->dtype == MOE_F32) {
     e = launch_ffn_simt(static_cast<const float*>(W.x_perm), offsets, nE, P, D->d, D->I,
@@ -152,13 +168,12 @@ moe_status do_ffn(const moe_layer_desc* D, const void* x, const int32_t* offsets
 
 // The same with Q8_0 expert weights (bf16 activations).
 moe_status do_ffn_q8(const moe_layer_desc* D, const void* x, const int32_t* offsets,
-                     const int32_t* tok_idx, const float* slot_w, const moe_q8_weight* Wg,
-                     const moe_q8_weight* Wu, const moe_q8_weight* Wd, void* y_perm, const Ws& W,
-                     cudaStream_t s) {
+                     const int32_t* tok_idx, const int32_t* slot_row, const float* slot_w,
+                     const moe_q8_weight* Wg, const moe_q8_weight* Wu, const moe_q8_weight* Wd,
+                     void* y_perm, const Ws& W, cudaStream_t s) {
   const int P = D->T * (D->k + D->S);
   const int nE = D->E + D->S;
-  if (launch_gather_rows_to_f16(x, tok_idx, offsets + nE, P, D->T, D->d, W.x_perm, W.flags, s) !=
-      cudaSuccess)
+  if (permute_rows(D, true, x, offsets, tok_idx, slot_row, W, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   const Q8Weight g{Wg->q, Wg->scale}, u{Wu->q, Wu->scale}, dn{Wd->q, Wd->scale};
   return cuda_status(launch_ffn_tc_q8(W.x_perm, offsets, nE, P, D->d, D->I, (double)P / nE, g, u,
@@ -319,8 +334,8 @@ moe_status moe_expert_ffn(const moe_layer_desc* desc, const void* x,
     return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
   const Ws W = carve(workspace, ws_layout(*desc));
-  return do_ffn(desc, x, expert_offsets, token_indices, slot_w, Wg, Wu, Wd, y_perm, W,
-                static_cast<cudaStream_t>(stream));
+  return do_ffn(desc, x, expert_offsets, token_indices, nullptr, slot_w, Wg, Wu, Wd, y_perm,
+                W, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_combine(const moe_layer_desc* desc, const void* y_perm, const int32_t* slot_row,
@@ -361,8 +376,8 @@ moe_status moe_expert_ffn_q8(const moe_layer_desc* desc, const void* x,
     return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
   const Ws W = carve(workspace, ws_layout(*desc));
-  return do_ffn_q8(desc, x, expert_offsets, token_indices, slot_w, Wg, Wu, Wd, y_perm, W,
-                   static_cast<cudaStream_t>(stream));
+  return do_ffn_q8(desc, x, expert_offsets, token_indices, nullptr, slot_w, Wg, Wu, Wd, y_perm,
+                   W, static_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_layer_forward_q8(const moe_layer_desc* desc, const void* x, const void* Wr,
@@ -391,7 +406,8 @@ moe_status moe_layer_forward_q8(const moe_layer_desc* desc, const void* x, const
                   W.slot_row, W.active, W.n_active, nullptr, W.bits, W.wpre, W.counts, W.flags,
                   s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if ((st = do_ffn_q8(desc, x, W.offsets, W.tok_idx, nullptr, Wg, Wu, Wd, W.y_perm, W, s)) !=
+  if ((st = do_ffn_q8(desc, x, W.offsets, W.tok_idx, W.slot_row, nullptr, Wg, Wu, Wd, W.y_perm,
+                      W, s)) !=
       MOE_OK)
     return st;
   return cuda_status(launch_combine(desc->dtype, W.y_perm, W.slot_row, w, residual, desc->T,
@@ -441,7 +457,8 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
                   W.slot_row, W.active, W.n_active, nullptr, W.bits, W.wpre, W.counts, W.flags,
                   s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if ((st = do_ffn(desc, x, W.offsets, W.tok_idx, nullptr, Wg, Wu, Wd, W.y_perm, W, s)) != MOE_OK)
+  if ((st = do_ffn(desc, x, W.offsets, W.tok_idx, W.slot_row, nullptr, Wg, Wu, Wd, W.y_perm, W,
+                   s)) != MOE_OK)
     return st;
   return cuda_status(launch_combine(desc->dtype, W.y_perm, W.slot_row, w, residual, desc->T,
                                     desc->d, desc->k, desc->S, y, s));

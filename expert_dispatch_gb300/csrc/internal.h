@@ -104,6 +104,12 @@ cudaError_t launch_gather_rows_to_f16(const void* x, const int32_t* tok_idx,
                                       const int32_t* total_rows, int P, int T, int d,
                                       void* x_perm, int* flags, cudaStream_t s);
 
+// x_perm[slot_row[t, j]] = x[t] for every token t and slot j (dropped slots,
+// -1, skipped); to_f16: bf16 rows written as fp16 rows
+cudaError_t launch_scatter_rows(int dtype, bool to_f16, const void* x, const int32_t* slot_row,
+                                const int32_t* total_rows, int T, int ks, int d, void* x_perm,
+                                int* flags, cudaStream_t s);
+
 cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* tok_idx,
                                const int32_t* total_rows, int P, int T, int d, void* x_perm,
                                int* flags, cudaStream_t s);

@@ -5,6 +5,11 @@
 //               "send (cur rows, local_ids) to the worker" step of the layer
 //               pseudocode in "Expert-Sharded Swarm Inference: The Design",
 //               done as an in-HBM permutation).
+// scatter_rows: the same permutation driven from the token side: x[t] is
+//               read once and written to x_perm[slot_row[t, j]] for each of
+//               its k + S slots, so a token row crosses HBM once however
+//               many experts it is routed to (the row gather reads it once
+//               per slot, from DRAM whenever x does not stay in L2).
 // combine     : y[t] = sum_{j<k} w[t,j] * y_perm[slot_row[t,j]]
 //                      + sum_{s<S} y_perm[slot_row[t,k+s]] (+ residual[t]),
 //               in that fixed order, fp32 ("Distributed MoE" (tenzro docs),
@@ -76,6 +81,79 @@ __global__ void gather_rows_to_f16_kernel(const uint4* __restrict__ x,
     dst[v] = out;
   }
   if (__any_sync(0xffffffffu, overflow) && lane == 0) flag_error(flags, kErrDeviceInput);
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// bf16 x 8 -> fp16 x 8; sets `overflow` for a value beyond fp16's range.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 in, bool& overflow) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&in);
+  uint4 out;
+  uint32_t* o = reinterpret_cast<uint32_t*>(&out);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(b[i]);
+    overflow |= fabsf(f.x) > 65504.f || fabsf(f.y) > 65504.f;
+    const __half2 h = __floats2half2_rn(f.x, f.y);
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return out;
+}
+
+constexpr int kScatterThreads = 256;
+constexpr int kScatterBatch = 8;      // 16-byte vectors in flight per thread
+constexpr int kScatterMaxSlots = 36;  // k <= 32, S <= 4
+
+// Block per token t: its slot rows are staged in shared memory (a dropped
+// slot, -1, is skipped; a row outside the batch rows is flagged and
+// skipped), then each thread loads up to kScatterBatch 16-byte vectors of
+// x[t] and stores them to every slot row.  TO_F16: bf16 in, fp16 out.
+template <bool TO_F16>
+__global__ void __launch_bounds__(kScatterThreads)
+    scatter_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ slot_row,
+                        const int32_t* __restrict__ total_rows, int ks, int vec_per_row,
+                        uint4* __restrict__ x_perm, int* flags) {
+  pdl_wait();     // the predecessor grid is complete and visible
+  pdl_trigger();  // dependents may launch (they wait for this grid in turn)
+  __shared__ int rows_s[kScatterMaxSlots];
+  const int t = blockIdx.x;
+  if (threadIdx.x < ks) {
+    const int r = slot_row[(size_t)t * ks + threadIdx.x];
+    const bool bad = r >= *total_rows || r < -1;
+    if (bad) flag_error(flags, kErrDeviceInput);
+    rows_s[threadIdx.x] = bad ? -1 : r;
+  }
+  __syncthreads();
+  const uint4* src = x + (size_t)t * vec_per_row;
+  bool overflow = false;
+  for (int v0 = threadIdx.x; v0 < vec_per_row; v0 += kScatterThreads * kScatterBatch) {
+    uint4 buf[kScatterBatch];
+#pragma unroll
+    for (int i = 0; i < kScatterBatch; ++i) {
+      const int v = v0 + kScatterThreads * i;
+      if (v < vec_per_row) {
+        buf[i] = ld_stream(src + v);
+        if (TO_F16) buf[i] = bf16x8_to_f16x8(buf[i], overflow);
+      }
+    }
+    for (int j = 0; j < ks; ++j) {
+      const int r = rows_s[j];
+      if (r < 0) continue;
+      uint4* dst = x_perm + (size_t)r * vec_per_row;
+#pragma unroll
+      for (int i = 0; i < kScatterBatch; ++i) {
+        const int v = v0 + kScatterThreads * i;
+        if (v < vec_per_row) dst[v] = buf[i];
+      }
+    }
+  }
+  if (TO_F16 && __syncthreads_or(overflow) && threadIdx.x == 0) flag_error(flags, kErrDeviceInput);
 }
 
 __device__ __forceinline__ void add8(float (&acc)[8], uint4 v, float w) {
@@ -253,6 +331,19 @@ cudaError_t launch_gather_rows_to_f16(const void* x, const int32_t* tok_idx,
   (void)launch_kernel(gather_rows_to_f16_kernel, (P + 7) / 8, 256, 0, s,
                       static_cast<const uint4*>(x), tok_idx, total_rows, P, T, d / 8,
                       static_cast<uint4*>(x_perm), flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_rows(int dtype, bool to_f16, const void* x, const int32_t* slot_row,
+                                const int32_t* total_rows, int T, int ks, int d, void* x_perm,
+                                int* flags, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (ks > kScatterMaxSlots) return cudaErrorInvalidValue;
+  const int vec = (int)(d * dtype_size(dtype) / 16);
+  ProfScope pr("scatter_rows", s);
+  auto kern = to_f16 ? scatter_rows_kernel<true> : scatter_rows_kernel<false>;
+  (void)launch_kernel(kern, T, kScatterThreads, 0, s, static_cast<const uint4*>(x), slot_row,
+                      total_rows, ks, vec, static_cast<uint4*>(x_perm), flags);
   return cudaGetLastError();
 }
 

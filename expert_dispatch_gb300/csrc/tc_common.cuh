@@ -161,21 +161,25 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, i
 // Epilogue, run by the kEpiWarps epilogue warps (warp indices first_warp ..
 // first_warp + 7): for every unit of this CTA, wait for its accumulators in
 // TMEM, read them with tcgen05.ld (a warp may only read its lane quarter,
-// warp % 4; the two warps of a quarter take alternate 16-column chunks),
-// apply the mode's epilogue and store, then hand the TMEM buffer back.
+// warp % 4; the two warps of a quarter take alternate 16-column chunks) and
+// apply the mode's epilogue.
+//   MODE_ROUTER : partial logits, fp32, stored straight from the loads
+//   MODE_GATEUP : H = silu(gate) * up, bf16 (fp16 when H_F16; a value beyond
+//                 fp16's range is flagged as an input error)
+//   MODE_DOWN   : y_perm = acc * row_scale, bf16 (whatever H_F16)
+// For the last two the whole unit is first turned into packed 16-bit pairs
+// held in registers; the TMEM buffer is handed back before the global
+// stores, so those overlap the next unit's MMAs instead of delaying them.
 // With NPART = 2 the unit's K blocks were accumulated into two partial sets
 // (even and odd K blocks of the unit, NACC * BN columns apart), added here
 // in that order; a unit with a single K block has only the first.
-//   MODE_ROUTER : partial logits, fp32
-//   MODE_GATEUP : H = silu(gate) * up, bf16 (fp16 when H_F16; a value beyond
-//                 fp16's range is flagged as an input error)
-//   MODE_DOWN   : y_perm = acc * row_scale, bf16
 template <int MODE, int BN, int NACC, int NBUF, bool H_F16 = false, int NPART = 1>
 __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_tiles, int KB,
                                               const int* prefix, const int* gstart,
                                               uint32_t tmem_base, uint32_t accf0,
                                               uint32_t acce0, volatile int* abort_flag,
                                               int first_warp) {
+  constexpr int NCH = BN / 32;  // 16-column chunks per thread
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                   // TMEM lane quarter this warp may access
   const int half = (warp - first_warp) / 4;  // alternate 16-column chunks
@@ -191,8 +195,8 @@ __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_
     const uint32_t tb =
         tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NPART * NACC * BN);
     const bool two = NPART == 2 && t.kb1 - t.kb0 >= 2;
-    for (int c0 = 16 * half; c0 < t.nt; c0 += 32) {
-      uint32_t a[16], b[16];
+    // accumulator columns c0 .. c0 + 15 (both operands, partial sets added)
+    auto load16 = [&](int c0, uint32_t (&a)[16], uint32_t (&b)[16]) {
       tmem_ld16(tb + c0, a);
       if (NACC == 2) tmem_ld16(tb + BN + c0, b);
       if (two) {
@@ -207,35 +211,76 @@ __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_
         }
       }
       tmem_ld_wait();
-      if (mvalid) {
+    };
+    if constexpr (MODE == MODE_ROUTER) {
+      for (int c0 = 16 * half; c0 < t.nt; c0 += 32) {
+        uint32_t a[16], b[16];
+        load16(c0, a, b);
+        if (!mvalid) continue;
+        const size_t chunk = (size_t)(t.kb0 / p.kb_per);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int col = c0 + j;
           if (col >= t.nt) break;
           const size_t row = (size_t)(t.r0 + col);
-          const float v = __uint_as_float(a[j]);
-          if (MODE == MODE_ROUTER) {
-            const size_t chunk = (size_t)(t.kb0 / p.kb_per);
-            static_cast<float*>(p.out)[(chunk * p.rows_single + row) * p.ldo + m] = v;
-          } else if (MODE == MODE_GATEUP) {
-            const float hval = silu_f32(v) * __uint_as_float(b[j]);
-            if (H_F16) {
-              const __half hh = __float2half_rn(hval);
-              if (__hisinf(hh)) flag_error(p.err, kErrDeviceInput);
-              static_cast<__half*>(p.out)[row * p.ldo + m] = hh;
-            } else {
-              static_cast<__nv_bfloat16*>(p.out)[row * p.ldo + m] = __float2bfloat16_rn(hval);
-            }
+          static_cast<float*>(p.out)[(chunk * p.rows_single + row) * p.ldo + m] =
+              __uint_as_float(a[j]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8u * buf);
+    } else {
+      uint32_t pk[NCH][8];  // the unit's results, packed 16-bit pairs
+#pragma unroll
+      for (int i = 0; i < NCH; ++i) {
+        const int c0 = 16 * half + 32 * i;
+        if (c0 >= t.nt) break;  // warp-uniform
+        uint32_t a[16], b[16];
+        load16(c0, a, b);
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          float v0 = __uint_as_float(a[j]), v1 = __uint_as_float(a[j + 1]);
+          if (MODE == MODE_GATEUP) {
+            v0 = silu_f32(v0) * __uint_as_float(b[j]);
+            v1 = silu_f32(v1) * __uint_as_float(b[j + 1]);
+          } else if (p.row_scale) {
+            const int col = c0 + j;  // row_scale is read for batch rows only
+            if (col < t.nt) v0 *= p.row_scale[t.r0 + col];
+            if (col + 1 < t.nt) v1 *= p.row_scale[t.r0 + col + 1];
+          }
+          if (H_F16 && MODE == MODE_GATEUP) {
+            const __half2 h = __floats2half2_rn(v0, v1);
+            const bool inf0 = c0 + j < t.nt && __hisinf(__low2half(h));
+            const bool inf1 = c0 + j + 1 < t.nt && __hisinf(__high2half(h));
+            if (mvalid && (inf0 || inf1)) flag_error(p.err, kErrDeviceInput);
+            pk[i][j / 2] = *reinterpret_cast<const uint32_t*>(&h);
           } else {
-            const float sc = p.row_scale ? p.row_scale[row] : 1.f;
-            static_cast<__nv_bfloat16*>(p.out)[row * p.ldo + m] = __float2bfloat16_rn(v * sc);
+            const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+            pk[i][j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8u * buf);  // TMEM free: stores follow
+      if (mvalid) {
+        uint16_t* out = static_cast<uint16_t*>(p.out);
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+          const int c0 = 16 * half + 32 * i;
+          if (c0 >= t.nt) break;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = c0 + j;
+            if (col >= t.nt) break;
+            const uint32_t w = pk[i][j / 2];
+            out[(size_t)(t.r0 + col) * p.ldo + m] =
+                (uint16_t)((j & 1) ? (w >> 16) : (w & 0xffffu));
           }
         }
       }
     }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(acce0 + 8u * buf);
   }
 }
 
