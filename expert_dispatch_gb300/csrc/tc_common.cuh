@@ -165,7 +165,7 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, i
 // apply the mode's epilogue.
 //   MODE_ROUTER : partial logits, fp32, stored straight from the loads
 //   MODE_GATEUP : H = silu(gate) * up, bf16 (fp16 when H_F16; a value beyond
-//                 fp16's range is flagged as an input error)
+//                 fp16's range is flagged as an input error); silu_fast
 //   MODE_DOWN   : y_perm = acc * row_scale, bf16 (whatever H_F16)
 // For the last two the whole unit is first turned into packed 16-bit pairs
 // held in registers; the TMEM buffer is handed back before the global
@@ -242,8 +242,8 @@ __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_
         for (int j = 0; j < 16; j += 2) {
           float v0 = __uint_as_float(a[j]), v1 = __uint_as_float(a[j + 1]);
           if (MODE == MODE_GATEUP) {
-            v0 = silu_f32(v0) * __uint_as_float(b[j]);
-            v1 = silu_f32(v1) * __uint_as_float(b[j + 1]);
+            v0 = silu_fast(v0) * __uint_as_float(b[j]);
+            v1 = silu_fast(v1) * __uint_as_float(b[j + 1]);
           } else if (p.row_scale) {
             const int col = c0 + j;  // row_scale is read for batch rows only
             if (col < t.nt) v0 *= p.row_scale[t.r0 + col];
