@@ -273,6 +273,57 @@ int num_sms() {
 
 using namespace moe;
 
+// The expert tier: host-resident expert projections, a pool of HBM slots and
+// the slot cache deciding residency (slot_cache.cu).
+struct moe_expert_tier {
+  moe_layer_desc desc{};
+  int device = 0;
+  int nE = 0, n_slots = 0;
+  size_t mat_bytes = 0;  // one expert's Wg (= Wu = Wd) bytes
+  const uint8_t* host[3] = {nullptr, nullptr, nullptr};
+  bool registered[3] = {false, false, false};
+  void* pool[3] = {nullptr, nullptr, nullptr};  // Wg, Wu, Wd slots
+  int32_t* host_tab = nullptr;  // pinned: [nE + 1] batch bounds, then [nE][nE] pass tables
+  int32_t* dev_tab = nullptr;   // [nE][nE] pass tables
+  cudaEvent_t done = nullptr;
+  bool done_recorded = false;
+  uint64_t bytes_loaded = 0;
+  SlotCache cache;
+  std::mutex mu;
+  moe_expert_tier(int slots, int experts) : cache(slots, experts) {}
+};
+
+namespace {
+
+void tier_free(moe_expert_tier* t) {
+  if (!t) return;
+  if (t->done) {
+    if (t->done_recorded) cudaEventSynchronize(t->done);
+    cudaEventDestroy(t->done);
+  }
+  for (int i = 0; i < 3; ++i) {
+    if (t->pool[i]) cudaFree(t->pool[i]);
+    if (t->registered[i]) cudaHostUnregister(const_cast<uint8_t*>(t->host[i]));
+  }
+  if (t->dev_tab) cudaFree(t->dev_tab);
+  if (t->host_tab) cudaFreeHost(t->host_tab);
+  delete t;
+}
+
+// Copy expert e's three projections into `slot` (host -> device, on stream s).
+moe_status tier_load(moe_expert_tier* t, int e, int slot, cudaStream_t s) {
+  for (int i = 0; i < 3; ++i) {
+    if (cudaMemcpyAsync(static_cast<uint8_t*>(t->pool[i]) + (size_t)slot * t->mat_bytes,
+                        t->host[i] + (size_t)e * t->mat_bytes, t->mat_bytes,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  t->bytes_loaded += 3 * t->mat_bytes;
+  return MOE_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 moe_status moe_workspace_size(const moe_layer_desc* desc, size_t* bytes) {
@@ -462,6 +513,169 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
     return st;
   return cuda_status(launch_combine(desc->dtype, W.y_perm, W.slot_row, w, residual, desc->T,
                                     desc->d, desc->k, desc->S, y, s));
+}
+
+moe_status moe_tier_create(const moe_layer_desc* desc, const void* Wg_host, const void* Wu_host,
+                           const void* Wd_host, size_t hbm_budget_bytes, moe_expert_tier** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  moe_layer_desc D = desc ? *desc : moe_layer_desc{};
+  D.T = 1;  // the tier's shape check does not depend on T
+  moe_status st = check_desc(desc ? &D : nullptr);
+  if (st != MOE_OK) return st;
+  if (D.dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (!Wg_host || !Wu_host || !Wd_host) return MOE_ERR_INVALID_ARG;
+  const int nE = D.E + D.S;
+  const size_t mat_bytes = (size_t)D.I * D.d * 2;
+  const size_t slots = hbm_budget_bytes / (3 * mat_bytes);
+  if (slots < 1) return MOE_ERR_INVALID_ARG;
+  const int n_slots = slots > (size_t)nE ? nE : (int)slots;
+  moe_expert_tier* t = new moe_expert_tier(n_slots, nE);
+  t->desc = D;
+  t->nE = nE;
+  t->n_slots = n_slots;
+  t->mat_bytes = mat_bytes;
+  t->host[0] = static_cast<const uint8_t*>(Wg_host);
+  t->host[1] = static_cast<const uint8_t*>(Wu_host);
+  t->host[2] = static_cast<const uint8_t*>(Wd_host);
+  if (cudaGetDevice(&t->device) != cudaSuccess) {
+    tier_free(t);
+    return MOE_ERR_CUDA;
+  }
+  for (int i = 0; i < 3; ++i) {
+    // page-lock the host copy so that slot loads are asynchronous DMA; memory
+    // that is already page-locked is used as it is
+    const cudaError_t e = cudaHostRegister(const_cast<uint8_t*>(t->host[i]),
+                                           (size_t)nE * mat_bytes, cudaHostRegisterDefault);
+    if (e == cudaSuccess)
+      t->registered[i] = true;
+    else
+      (void)cudaGetLastError();
+    if (cudaMalloc(&t->pool[i], (size_t)n_slots * mat_bytes) != cudaSuccess) {
+      (void)cudaGetLastError();
+      tier_free(t);
+      return MOE_ERR_CUDA;
+    }
+  }
+  if (cudaHostAlloc(reinterpret_cast<void**>(&t->host_tab),
+                    ((size_t)nE + 1 + (size_t)nE * nE) * 4, cudaHostAllocDefault) !=
+          cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void**>(&t->dev_tab), (size_t)nE * nE * 4) != cudaSuccess ||
+      cudaEventCreateWithFlags(&t->done, cudaEventDisableTiming) != cudaSuccess) {
+    (void)cudaGetLastError();
+    tier_free(t);
+    return MOE_ERR_CUDA;
+  }
+  *out = t;
+  return MOE_OK;
+}
+
+moe_status moe_tier_destroy(moe_expert_tier* tier) {
+  tier_free(tier);
+  return MOE_OK;
+}
+
+moe_status moe_tier_get_stats(moe_expert_tier* tier, moe_tier_stats* out) {
+  if (!tier || !out) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(tier->mu);
+  tier->cache.fill_stats(out);
+  out->bytes_loaded = tier->bytes_loaded;
+  return MOE_OK;
+}
+
+moe_status moe_tier_prefetch(moe_expert_tier* tier, const int32_t* experts, int n, void* stream) {
+  if (!tier || n < 0 || (n > 0 && !experts)) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(tier->mu);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n > tier->n_slots) n = tier->n_slots;  // the rest could not stay resident anyway
+  if (n == 0) return MOE_OK;
+  std::vector<int32_t> slot(n), load(n), pass(n);
+  int32_t n_passes = 0;
+  if (!tier->cache.assign(experts, n, slot.data(), load.data(), pass.data(), &n_passes))
+    return MOE_ERR_INVALID_ARG;
+  if (tier->done_recorded && cudaStreamWaitEvent(s, tier->done, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  for (int i = 0; i < n; ++i) {
+    if (!load[i]) continue;
+    const moe_status st = tier_load(tier, experts[i], slot[i], s);
+    if (st != MOE_OK) return st;
+  }
+  if (cudaEventRecord(tier->done, s) != cudaSuccess) return MOE_ERR_CUDA;
+  tier->done_recorded = true;
+  return MOE_OK;
+}
+
+moe_status moe_tier_forward(moe_expert_tier* tier, const moe_layer_desc* desc, const void* x,
+                            const void* Wr, const float* logit_bias, const float* sel_bias,
+                            const float* residual, float* y, int32_t* topk_ids_out,
+                            float* topk_w_out, void* workspace, size_t ws_bytes, void* stream) {
+  if (!tier) return MOE_ERR_INVALID_ARG;
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  const moe_layer_desc& T0 = tier->desc;
+  if (desc->d != T0.d || desc->E != T0.E || desc->k != T0.k || desc->I != T0.I ||
+      desc->S != T0.S || desc->dtype != T0.dtype)
+    return MOE_ERR_INVALID_ARG;
+  if (desc->T == 0) return MOE_OK;
+  if (!x || !Wr || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wr) || !aligned16(y) || (residual && !aligned16(residual)) ||
+      (topk_ids_out && !aligned16(topk_ids_out)) || (topk_w_out && !aligned16(topk_w_out)))
+    return MOE_ERR_INVALID_ARG;
+  if (sel_bias && desc->gate != MOE_GATE_SIGMOID_BIAS) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
+  std::lock_guard<std::mutex> g(tier->mu);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Ws W = carve(workspace, ws_layout(*desc));
+  const int nE = tier->nE;
+  const int P = desc->T * (desc->k + desc->S);
+  int32_t* ids = topk_ids_out ? topk_ids_out : W.topk_ids;
+  float* w = topk_w_out ? topk_w_out : W.topk_w;
+  if (tier->done_recorded && cudaStreamWaitEvent(s, tier->done, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(W.flags, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((st = do_route(desc, x, Wr, logit_bias, sel_bias, ids, w, W, s)) != MOE_OK) return st;
+  if (launch_plan(ids, nullptr, desc->T, desc->E, desc->k, desc->S, W.offsets, W.tok_idx,
+                  W.slot_row, W.active, W.n_active, nullptr, W.bits, W.wpre, W.counts, W.flags,
+                  s) != cudaSuccess ||
+      permute_rows(desc, false, x, W.offsets, W.tok_idx, W.slot_row, W, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // the routing decision reaches the host: batch bounds per expert
+  int32_t* bounds = tier->host_tab;
+  if (cudaMemcpyAsync(bounds, W.offsets, (size_t)(nE + 1) * 4, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  std::vector<int32_t> active;
+  for (int e = 0; e < nE; ++e)
+    if (bounds[e + 1] > bounds[e]) active.push_back(e);
+  const int n = (int)active.size();
+  std::vector<int32_t> slot(n), load(n), pass(n);
+  int32_t n_passes = 0;
+  if (!tier->cache.assign(active.data(), n, slot.data(), load.data(), pass.data(), &n_passes))
+    return MOE_ERR_DEVICE_INPUT;  // batch bounds that are not a partition
+  const double mean_rows = (double)P / (double)nE;
+  for (int p = 0; p < n_passes; ++p) {
+    int32_t* tab = tier->host_tab + (nE + 1) + (size_t)p * nE;
+    for (int e = 0; e < nE; ++e) tab[e] = -1;
+    for (int i = 0; i < n; ++i)
+      if (pass[i] == p) tab[active[i]] = slot[i];
+    int32_t* dtab = tier->dev_tab + (size_t)p * nE;
+    if (cudaMemcpyAsync(dtab, tab, (size_t)nE * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    for (int i = 0; i < n; ++i)
+      if (pass[i] == p && load[i] && (st = tier_load(tier, active[i], slot[i], s)) != MOE_OK)
+        return st;
+    if (launch_ffn_tc(W.x_perm, W.offsets, nE, P, desc->d, desc->I, mean_rows, tier->pool[0],
+                      tier->pool[1], tier->pool[2], nullptr, W.h, W.y_perm, W.flags, s,
+                      tier->n_slots, dtab) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (launch_combine(desc->dtype, W.y_perm, W.slot_row, w, residual, desc->T, desc->d, desc->k,
+                     desc->S, y, s) != cudaSuccess ||
+      cudaEventRecord(tier->done, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  tier->done_recorded = true;
+  return MOE_OK;
 }
 
 moe_status moe_get_device_status(void* workspace, size_t ws_bytes, int clear, void* stream) {

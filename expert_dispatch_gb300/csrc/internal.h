@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -119,11 +121,13 @@ cudaError_t launch_ffn_simt(const float* x_perm, const int32_t* offsets, int n_g
                             int d, int I, const float* Wg, const float* Wu, const float* Wd,
                             const float* slot_w, float* h, float* y_perm, cudaStream_t s);
 
-// bf16 tcgen05 expert FFN (gate/up + SwiGLU, then down)
+// bf16 tcgen05 expert FFN (gate/up + SwiGLU, then down).  With group_slot,
+// group g's weights are matrix group_slot[g] of Wg/Wu/Wd, which then hold
+// n_mats matrices (a slot pool); a negative entry skips the group's rows.
 cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_groups, int P,
                           int d, int I, double mean_rows, const void* Wg, const void* Wu,
                           const void* Wd, const float* slot_w, void* h, void* y_perm, int* err,
-                          cudaStream_t s);
+                          cudaStream_t s, int n_mats = 0, const int32_t* group_slot = nullptr);
 
 cudaError_t launch_combine(int dtype, const void* y_perm, const int32_t* slot_row,
                            const float* topk_w, const float* residual, int T, int d, int k,
@@ -148,5 +152,32 @@ cudaError_t launch_combine_partial(int dtype, const void* y_perm, const int32_t*
                                    cudaStream_t s);
 
 int num_sms();
+
+// Expert residency in a bounded set of device slots (slot_cache.cu).
+class SlotCache {
+ public:
+  SlotCache(int n_slots, int n_experts);
+  // Slots for one step's distinct experts: slot[i], load[i] (1: its bytes
+  // must be brought into the slot), pass[i] (passes run in order); false on a
+  // bad argument (out of range or repeated expert), with nothing changed.
+  bool assign(const int32_t* experts, int n, int32_t* slot, int32_t* load, int32_t* pass,
+              int32_t* n_passes);
+  int slot_of(int expert) const { return expert_slot_[expert]; }
+  int n_slots() const { return (int)slot_expert_.size(); }
+  int n_experts() const { return (int)expert_slot_.size(); }
+  int resident() const;
+  void fill_stats(moe_tier_stats* out) const;
+
+ private:
+  int pick() const;
+  struct Counters {
+    uint64_t steps = 0, hits = 0, misses = 0, evictions = 0, extra_passes = 0;
+  };
+  std::vector<int> slot_expert_, expert_slot_;
+  std::vector<uint64_t> stamp_;  // step that last used the slot
+  std::vector<char> pinned_;
+  uint64_t clock_ = 0;
+  Counters stats_;
+};
 
 }  // namespace moe

@@ -30,7 +30,14 @@ struct Params {
   int max_rows;            // rows of the token operand / output; batch bounds are clamped to it
   int ksplit;              // MODE_ROUTER: K is cut into ksplit chunks of kb_per 64-wide blocks,
   int kb_per;              //   each chunk's partial sums go to out + chunk * rows * ldo
+  const int32_t* group_slot;  // [n_groups] weight matrix of each group (null: group g uses
+                              //   matrix g); a negative entry skips the group
 };
+
+// The weight matrix group g reads: its slot in a slot pool, or g itself.
+__device__ __forceinline__ int weight_mat(const Params& p, int g) {
+  return p.group_slot ? p.group_slot[g] : g;
+}
 
 struct Unit {
   int g, mt, r0, nt, kb0, kb1;
@@ -80,7 +87,8 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int*
 // safe first: each clamped to [0, max_rows] and forced non-decreasing
 // (running max), so every batch lies inside the row buffers whatever the
 // caller passed; any change is flagged.  Then prefix[g] = units before group
-// g, with m_tiles x ceil(rows / BN) (x ksplit for the router) units per group.
+// g, with m_tiles x ceil(rows / BN) (x ksplit for the router) units per group;
+// a group whose group_slot entry is negative gets none.
 template <int MODE, int BN>
 __device__ __forceinline__ void build_schedule(const Params& p, int m_tiles, int* prefix,
                                                int* gstart) {
@@ -108,7 +116,7 @@ __device__ __forceinline__ void build_schedule(const Params& p, int m_tiles, int
   for (int base = 0; base < p.n_groups; base += 32) {
     const int g = base + lane;
     int units = 0;
-    if (g < p.n_groups) {
+    if (g < p.n_groups && !(p.group_slot && p.group_slot[g] < 0)) {
       const int cnt = gstart[g + 1] - gstart[g];
       units = m_tiles * ((cnt + BN - 1) / BN) * (MODE == MODE_ROUTER ? p.ksplit : 1);
     }

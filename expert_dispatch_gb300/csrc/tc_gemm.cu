@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit t =
             tc::decode_unit<MODE, BN>(blockIdx.x, prefix, gstart, p.n_groups, m_tiles, KB, p);
         const uint32_t bytes = C::NA * C::A_BYTES + ((t.nt + 31) / 32) * 4096;
-        const int arow = t.g * p.Mg + t.mt * 128;
+        const int arow = tc::weight_mat(p, t.g) * p.Mg + t.mt * 128;
         n_pre = min(STAGES, t.kb1 - t.kb0);
         for (int i = 0; i < n_pre; ++i) {  // fresh ring: stages 0..n_pre-1 are free
           mbar_arrive_expect_tx(full_bar(i), bytes);
@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit t = tc::decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
         const int nchunks = (t.nt + 31) / 32;
         const uint32_t bytes = C::NA * C::A_BYTES + nchunks * 4096;
-        const int arow = t.g * p.Mg + t.mt * 128;
+        const int arow = tc::weight_mat(p, t.g) * p.Mg + t.mt * 128;
         bool ok = true;
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           const bool pre = first && kb - t.kb0 < n_pre;  // armed, weights already requested
@@ -327,7 +327,7 @@ int tc_row_capacity(int P) { return ((P + 31) / 32) * 32 + 256; }
 cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_groups, int P,
                           int d, int I, double mean_rows, const void* Wg, const void* Wu,
                           const void* Wd, const float* slot_w, void* h, void* y_perm, int* err,
-                          cudaStream_t s) {
+                          cudaStream_t s, int n_mats, const int32_t* group_slot) {
   if (P == 0) return cudaSuccess;
   const uint64_t cap = (uint64_t)tc_row_capacity(P);
   // Token tiles by mean batch size: 32 rows for decode-sized batches (deep
@@ -339,13 +339,14 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
   const int bn = small ? 32 : mean_rows <= 256.0 ? 128 : 256;
   // token operands: 32-row boxes for partial tiles, tile-high boxes for full ones
   CUtensorMap tg, tu, tx, txf, td, th, thf, thf2;
-  if (!make_tmap(&tg, Wg, d, (uint64_t)n_groups * I, 128) ||
-      !make_tmap(&tu, Wu, d, (uint64_t)n_groups * I, 128) ||
+  if (n_mats <= 0) n_mats = n_groups;
+  if (!make_tmap(&tg, Wg, d, (uint64_t)n_mats * I, 128) ||
+      !make_tmap(&tu, Wu, d, (uint64_t)n_mats * I, 128) ||
       !make_tmap(&tx, x_perm, d, cap, 32) || !make_tmap(&txf, x_perm, d, cap, bn) ||
-      !make_tmap(&td, Wd, I, (uint64_t)n_groups * d, 128) || !make_tmap(&th, h, I, cap, 32) ||
+      !make_tmap(&td, Wd, I, (uint64_t)n_mats * d, 128) || !make_tmap(&th, h, I, cap, 32) ||
       !make_tmap(&thf, h, I, cap, 32) || !make_tmap(&thf2, h, I, cap, 256))
     return cudaErrorInvalidValue;
-  Params p1{offsets, n_groups, 0, I, d, h, I, nullptr, err, P};
+  Params p1{offsets, n_groups, 0, I, d, h, I, nullptr, err, P, 0, 0, group_slot};
   const long long u1 = (long long)((I + 127) / 128) * ((P + bn - 1) / bn + n_groups);
   cudaError_t e;
   if (small)
@@ -356,7 +357,7 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
     e = launch_tc<MODE_GATEUP, 256, 3>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
   if (e != cudaSuccess) return e;
   const int bn2 = small ? 32 : 256;
-  Params p2{offsets, n_groups, 0, d, I, y_perm, d, slot_w, err, P};
+  Params p2{offsets, n_groups, 0, d, I, y_perm, d, slot_w, err, P, 0, 0, group_slot};
   const long long u2 = (long long)((d + 127) / 128) * ((P + bn2 - 1) / bn2 + n_groups);
   if (small) return launch_tc<MODE_DOWN, 32, 10>(td, td, th, thf, p2, u2, "ffn_down_tc", s);
   return launch_tc<MODE_DOWN, 256, 4>(td, td, th, thf2, p2, u2, "ffn_down_tc", s);

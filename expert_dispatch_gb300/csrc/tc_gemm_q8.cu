@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
       uint32_t phase = 0, armed = 0, armed_parity = 0;
       for (int u = blockIdx.x; u < total && !*abort_flag; u += gridDim.x) {
         const Unit t = tc::decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
-        const int arow = t.g * p.Mg + t.mt * 128;
+        const int mat = tc::weight_mat(p, t.g);
+        const int arow = mat * p.Mg + t.mt * 128;
         bool ok = true;
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           if (!mbar_wait(w_empty(stage), phase ^ 1u, abort_flag, p.err)) {
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
           mbar_arrive_expect_tx(bar, C::W_TX);
           armed |= 1u << stage;
           armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-          const int srow = t.g * sblocks + kb * 2;
+          const int srow = mat * sblocks + kb * 2;
           tma_load_2d(w, &tmQ0, bar, kb * 64, arow);
           tma_load_2d(w + C::SA_OFF, &tmS0, bar, t.mt * 128, srow);
           if (C::NA == 2) {

@@ -9,7 +9,8 @@ status.  There is no fallback: if libmoe.so is missing, every call raises.
 Entry points carry the C names: moe_workspace_size, moe_workspace_init,
 moe_route, moe_plan_dispatch, moe_expert_ffn, moe_combine, moe_layer_forward,
 moe_get_device_status, moe_status_string, moe_launch_count,
-moe_profile_enable, moe_profile_query.
+moe_profile_enable, moe_profile_query, the Q8_0 and no-alloc variants, the
+slot cache (moe_slot_cache_*) and the expert tier (moe_tier_*).
 """
 from __future__ import annotations
 
@@ -38,7 +39,10 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_d
             "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status",
             "moe_status_string", "moe_launch_count", "moe_profile_enable", "moe_profile_query",
             "moe_expert_ffn_noalloc", "moe_combine_partial", "moe_quantize_q8_0",
-            "moe_expert_ffn_q8", "moe_layer_forward_q8")
+            "moe_expert_ffn_q8", "moe_layer_forward_q8", "moe_slot_cache_create",
+            "moe_slot_cache_destroy", "moe_slot_cache_assign", "moe_slot_cache_slot_of",
+            "moe_slot_cache_get_stats", "moe_tier_create", "moe_tier_destroy",
+            "moe_tier_prefetch", "moe_tier_forward", "moe_tier_get_stats")
 
 
 class MoeError(RuntimeError):
@@ -58,6 +62,17 @@ class LayerDesc(ctypes.Structure):
 class Q8WeightStruct(ctypes.Structure):
     """moe_q8_weight"""
     _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
+
+
+class TierStats(ctypes.Structure):
+    """moe_tier_stats"""
+    _fields_ = [("steps", ctypes.c_uint64), ("hits", ctypes.c_uint64), ("misses", ctypes.c_uint64),
+                ("evictions", ctypes.c_uint64), ("extra_passes", ctypes.c_uint64),
+                ("bytes_loaded", ctypes.c_uint64), ("n_slots", ctypes.c_int32),
+                ("resident", ctypes.c_int32)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
 
 
 def make_desc(T, d, E, k, I, S=0, gate=MOE_GATE_SOFTMAX_TOPK, norm_topk=0, routed_scaling=1.0,
@@ -104,6 +119,19 @@ def lib():
     L.moe_quantize_q8_0.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
     L.moe_expert_ffn_q8.argtypes = [D, vp, vp, vp, vp, Q, Q, Q, vp, vp, sz, vp]
     L.moe_layer_forward_q8.argtypes = [D, vp, vp, vp, vp, Q, Q, Q, vp, vp, vp, vp, vp, sz, vp]
+    vpp = ctypes.POINTER(ctypes.c_void_p)
+    ip = ctypes.POINTER(ctypes.c_int32)
+    TS = ctypes.POINTER(TierStats)
+    L.moe_slot_cache_create.argtypes = [i32, i32, vpp]
+    L.moe_slot_cache_destroy.argtypes = [vp]
+    L.moe_slot_cache_assign.argtypes = [vp, vp, i32, vp, vp, vp, ip]
+    L.moe_slot_cache_slot_of.argtypes = [vp, i32, ip]
+    L.moe_slot_cache_get_stats.argtypes = [vp, TS]
+    L.moe_tier_create.argtypes = [D, vp, vp, vp, sz, vpp]
+    L.moe_tier_destroy.argtypes = [vp]
+    L.moe_tier_prefetch.argtypes = [vp, vp, i32, vp]
+    L.moe_tier_forward.argtypes = [vp, D, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_tier_get_stats.argtypes = [vp, TS]
     L.moe_profile_enable.argtypes = [i32]
     L.moe_profile_query.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
                                     ctypes.POINTER(ctypes.c_float)]
@@ -403,6 +431,120 @@ def moe_profile_query(kernel: str):
     _check(lib().moe_profile_query(kernel.encode(), ctypes.byref(n), ctypes.byref(ms)),
            "moe_profile_query")
     return n.value, ms.value
+
+
+# ---------------------------------------------------------------- slot cache and expert tier
+class SlotCache:
+    """moe_slot_cache: expert residency over n_slots slots (host only)."""
+
+    def __init__(self, n_slots: int, n_experts: int):
+        h = ctypes.c_void_p()
+        _check(lib().moe_slot_cache_create(n_slots, n_experts, ctypes.byref(h)),
+               "moe_slot_cache_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().moe_slot_cache_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def assign(self, experts):
+        """(slot, load, pass, n_passes) for one step's distinct experts."""
+        import numpy as np
+        e = np.ascontiguousarray(np.asarray(experts, dtype=np.int32))
+        n = e.size
+        slot, load, pas = (np.empty(n, np.int32) for _ in range(3))
+        npass = ctypes.c_int32(0)
+        ptr = lambda a: a.ctypes.data if n else None
+        _check(lib().moe_slot_cache_assign(self._h, ptr(e), n, ptr(slot), ptr(load), ptr(pas),
+                                           ctypes.byref(npass)), "moe_slot_cache_assign")
+        return slot, load, pas, npass.value
+
+    def slot_of(self, expert: int) -> int:
+        s = ctypes.c_int32(0)
+        _check(lib().moe_slot_cache_slot_of(self._h, expert, ctypes.byref(s)),
+               "moe_slot_cache_slot_of")
+        return s.value
+
+    def stats(self) -> dict:
+        st = TierStats()
+        _check(lib().moe_slot_cache_get_stats(self._h, ctypes.byref(st)),
+               "moe_slot_cache_get_stats")
+        return st.as_dict()
+
+
+def _host_p(t, dtype, what):
+    """Pointer of a contiguous host (CPU) tensor."""
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError("%s must be a CPU tensor" % what)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % what)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (what, dtype, t.dtype))
+    return t.data_ptr()
+
+
+class ExpertTier:
+    """moe_expert_tier: expert projections kept in host memory (Wg/Wu/Wd CPU bf16
+    tensors, kept alive here), a bounded pool of expert slots in HBM, and a
+    forward() that calls moe_tier_forward.  Wr and the biases are device tensors."""
+
+    def __init__(self, desc: LayerDesc, Wr, Wg_host, Wu_host, Wd_host, hbm_budget_bytes: int,
+                 logit_bias=None, sel_bias=None):
+        nE = desc.E + desc.S
+        for name, W, shape in (("Wg", Wg_host, (nE, desc.I, desc.d)),
+                               ("Wu", Wu_host, (nE, desc.I, desc.d)),
+                               ("Wd", Wd_host, (nE, desc.d, desc.I))):
+            _need(W, shape, name)
+        self.desc = desc
+        self.host = (Wg_host, Wu_host, Wd_host)
+        self.Wr, self.logit_bias, self.sel_bias = Wr, logit_bias, sel_bias
+        h = ctypes.c_void_p()
+        _check(lib().moe_tier_create(
+            ctypes.byref(desc), _host_p(Wg_host, torch.bfloat16, "Wg"),
+            _host_p(Wu_host, torch.bfloat16, "Wu"), _host_p(Wd_host, torch.bfloat16, "Wd"),
+            int(hbm_budget_bytes), ctypes.byref(h)), "moe_tier_create")
+        self._h = h
+        self.ws = alloc_workspace(desc, device=Wr.device)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().moe_tier_destroy(self._h)
+            self._h = None
+
+    __del__ = close
+
+    def prefetch(self, experts, stream=None):
+        import numpy as np
+        e = np.ascontiguousarray(np.asarray(experts, dtype=np.int32))
+        _check(lib().moe_tier_prefetch(self._h, e.ctypes.data if e.size else None, e.size,
+                                       _stream(stream)), "moe_tier_prefetch")
+
+    def forward(self, x, residual=None, y=None, topk_ids=None, topk_w=None, desc=None,
+                stream=None):
+        d = desc if desc is not None else self.desc
+        if d.T > self.desc.T:  # the workspace is sized for the tier's T
+            raise ValueError("T %d exceeds the tier's %d" % (d.T, self.desc.T))
+        _need(x, (d.T, d.d), "x")
+        if y is None:
+            y = torch.empty((d.T, d.d), dtype=torch.float32, device=x.device)
+        _need(y, (d.T, d.d), "y")
+        st = lib().moe_tier_forward(
+            self._h, ctypes.byref(d), _p(x, torch.bfloat16, "x"),
+            _p(self.Wr, torch.bfloat16, "Wr"), _p(self.logit_bias, torch.float32, "logit_bias"),
+            _p(self.sel_bias, torch.float32, "sel_bias"), _p(residual, torch.float32, "residual"),
+            _p(y, torch.float32, "y"), _p(topk_ids, torch.int32, "topk_ids_out"),
+            _p(topk_w, torch.float32, "topk_w_out"), _p(self.ws, torch.uint8, "workspace"),
+            self.ws.numel(), _stream(stream))
+        _check(st, "moe_tier_forward")
+        return y
+
+    def stats(self) -> dict:
+        st = TierStats()
+        _check(lib().moe_tier_get_stats(self._h, ctypes.byref(st)), "moe_tier_get_stats")
+        return st.as_dict()
 
 
 # ---------------------------------------------------------------- convenience

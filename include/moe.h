@@ -257,6 +257,80 @@ moe_status moe_layer_forward_q8(const moe_layer_desc* desc, const void* x, const
                                 int32_t* topk_ids_out, float* topk_w_out, void* workspace,
                                 size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------- expert tier in host memory
+   ("Distributed MoE", expert-residency paragraph: experts are kept in a
+   byte-bounded, least-recently-used memory tier over a colder tier, and
+   before a forward dispatches, readahead brings in the experts the routing
+   decision selected; "Module expert_store" (ferrox-core docs), design list:
+   a lease pins an entry against eviction while work still reads it, and a
+   step whose experts do not all fit still succeeds, at the cost of more
+   transfers.)
+   Here the colder tier is host memory (on GB300 the Grace memory, read over
+   NVLink-C2C) and the bounded tier is a pool of expert slots in HBM. */
+typedef struct {
+  uint64_t steps;         /* assignments made (forwards and prefetches) */
+  uint64_t hits;          /* experts already resident when a step needed them */
+  uint64_t misses;        /* experts brought into a slot */
+  uint64_t evictions;     /* resident experts displaced to make room */
+  uint64_t extra_passes;  /* FFN passes beyond the first: a step needed more experts than slots */
+  uint64_t bytes_loaded;  /* host -> device weight bytes (a bare slot cache reports 0) */
+  int32_t n_slots;
+  int32_t resident;       /* slots holding an expert */
+} moe_tier_stats;
+
+/* The residency logic on its own (host only, no device needed).  A cache of
+   n_slots slots over experts 0 .. n_experts-1 (1 <= n_slots <= n_experts).
+   moe_slot_cache_assign gives one step's n distinct experts their slots:
+   slot[i]; load[i] = 1 when expert i's bytes must be brought into that slot
+   (a miss), 0 when it is resident (a hit); pass[i], the pass that uses it.
+   Pass 0 holds every hit and as many misses as fit; a miss takes a free
+   slot, else the least recently used slot not pinned by the current pass
+   (its expert is evicted); when every slot is pinned, a new pass starts and
+   the pins are dropped.  Passes must run one after another.  *n_passes is
+   the number of passes (0 for n = 0).  A repeated or out-of-range expert is
+   MOE_ERR_INVALID_ARG with the cache unchanged.  Thread-safe per cache.
+   moe_slot_cache_slot_of: an expert's slot, or -1 when not resident. */
+typedef struct moe_slot_cache moe_slot_cache;
+moe_status moe_slot_cache_create(int n_slots, int n_experts, moe_slot_cache** out);
+moe_status moe_slot_cache_destroy(moe_slot_cache* cache);
+moe_status moe_slot_cache_assign(moe_slot_cache* cache, const int32_t* experts, int n,
+                                 int32_t* slot, int32_t* load, int32_t* pass,
+                                 int32_t* n_passes);
+moe_status moe_slot_cache_slot_of(moe_slot_cache* cache, int expert, int32_t* slot);
+moe_status moe_slot_cache_get_stats(moe_slot_cache* cache, moe_tier_stats* out);
+
+/* The expert tier.  moe_tier_create keeps pointers to the layer's expert
+   projections in HOST memory (bf16, layouts as in moe_layer_forward:
+   Wg/Wu [E+S, I, d], Wd [E+S, d, I]); the caller keeps them alive and
+   unchanged until moe_tier_destroy.  The tier page-locks them if they are
+   not already (and unlocks what it locked on destroy), and allocates
+   n_slots = min(E+S, floor(hbm_budget_bytes / (6 I d))) expert slots in
+   HBM on the current device (MOE_ERR_INVALID_ARG below one slot).  desc
+   fixes d, E, k, I, S, gate and dtype (MOE_BF16 only; other dtypes are
+   MOE_ERR_UNSUPPORTED); its T is ignored.
+
+   moe_tier_forward is moe_layer_forward over the tier, with desc giving
+   this call's T: route and plan on the device; the routing decision (the
+   expert batch sizes) is copied to the host, which WAITS for the stream
+   once; slots are assigned (moe_slot_cache_assign), the missing experts
+   are copied into their slots on `stream`, and the FFN runs once per pass
+   over the experts of that pass; then the combine.  The result equals
+   moe_layer_forward's bit for bit.  Calls on one tier are serialized
+   (the tier orders its work after its previous call's, whatever stream).
+   moe_tier_prefetch brings up to n_slots of the listed experts in ahead of
+   use (a caller-supplied hotlist), asynchronously on `stream`.
+   moe_tier_destroy waits for the tier's outstanding work. */
+typedef struct moe_expert_tier moe_expert_tier;
+moe_status moe_tier_create(const moe_layer_desc* desc, const void* Wg_host, const void* Wu_host,
+                           const void* Wd_host, size_t hbm_budget_bytes, moe_expert_tier** out);
+moe_status moe_tier_destroy(moe_expert_tier* tier);
+moe_status moe_tier_prefetch(moe_expert_tier* tier, const int32_t* experts, int n, void* stream);
+moe_status moe_tier_forward(moe_expert_tier* tier, const moe_layer_desc* desc, const void* x,
+                            const void* Wr, const float* logit_bias, const float* sel_bias,
+                            const float* residual, float* y, int32_t* topk_ids_out,
+                            float* topk_w_out, void* workspace, size_t ws_bytes, void* stream);
+moe_status moe_tier_get_stats(moe_expert_tier* tier, moe_tier_stats* out);
+
 /* Synchronizes `stream`, then reports the sticky device flag held in the
    workspace: MOE_OK, MOE_ERR_DEVICE_INPUT or MOE_ERR_TIMEOUT (MOE_ERR_CUDA if
    the copy itself fails).  clear != 0 resets the flag afterwards.          */
@@ -274,8 +348,9 @@ int64_t moe_launch_count(void);
    synchronizes on the recorded events and returns, for the named kernel, the
    number of recorded launches and their summed device time in milliseconds.
    Kernel names: router_logits_splitk, router_logits_tc, router_topk,
-   plan_small, plan_mark, plan_scan, plan_place, gather_rows, ffn_gateup_simt,
-   ffn_down_simt, ffn_gateup_tc, ffn_down_tc, combine, combine_partial.      */
+   plan_small, plan_mark, plan_scan, plan_place, gather_rows, scatter_rows,
+   ffn_gateup_simt, ffn_down_simt, ffn_gateup_tc, ffn_down_tc,
+   ffn_gateup_tc_q8, ffn_down_tc_q8, quantize_q8_0, combine, combine_partial. */
 moe_status moe_profile_enable(int on);
 moe_status moe_profile_query(const char* kernel, int32_t* launches, float* total_ms);
 
