@@ -367,6 +367,115 @@ def run_gpu(args, rank, world):
     return out
 
 
+# ---------------------------------------------------------------- the expert tier
+def host_link_gbs(dev, n_bytes=1 << 30, reps=3):
+    """Host (page-locked) -> device copy bandwidth, best of `reps` copies."""
+    h = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(n_bytes, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(reps + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        d.copy_(h, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, n_bytes / (a.elapsed_time(b) / 1e3) / 1e9)
+    del h, d
+    return best
+
+
+def run_tier(args, rank, world):
+    """The layer through the expert tier: expert projections in page-locked host
+    memory, args.tier_slots expert slots in HBM.  Steps cycle through
+    args.tier_inputs different token batches so that routing changes from step
+    to step and the slots churn.  Each step waits once on the host for the
+    routing decision (inside moe_tier_forward), so the timed region is the
+    stream's elapsed time around steps issued back to back."""
+    cfg = workload(args.workload, args.T, args.E)
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from expert_dispatch_gb300 import build
+    if rank == 0 or not os.path.exists(moe.LIB_PATH):
+        build.build()
+    inp = make_inputs(cfg, seed=args.seed + rank, device=dev)
+    desc = moe.desc_from_config(cfg)
+    host_w = []
+    for n in ("Wg", "Wu", "Wd"):
+        h = torch.empty(inp[n].shape, dtype=inp[n].dtype, pin_memory=True)
+        h.copy_(inp[n])
+        host_w.append(h)
+    expert_bytes = 3 * cfg.I * cfg.d * 2
+    tier = moe.ExpertTier(desc, inp["Wr"], *host_w, args.tier_slots * expert_bytes,
+                          logit_bias=inp["logit_bias"], sel_bias=inp["sel_bias"])
+    layer = moe.MoeLayer(desc, inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"],
+                         logit_bias=inp["logit_bias"], sel_bias=inp["sel_bias"])
+    g = torch.Generator(device=dev).manual_seed(args.seed + 100)
+    xs = [torch.randn((cfg.T, cfg.d), generator=g, device=dev).to(torch.bfloat16)
+          for _ in range(args.tier_inputs)]
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream()
+
+    def timed(fn, steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(steps):
+                fn(xs[i % len(xs)])
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    # the same steps with every expert resident in HBM (the tier's floor)
+    timed(lambda x: layer.forward(x, y=y), args.warmup)
+    resident_ms = timed(lambda x: layer.forward(x, y=y), args.steps)
+    link = host_link_gbs(dev)
+    timed(lambda x: tier.forward(x, y=y), args.warmup)
+    s0 = tier.stats()
+    sampler = ClockSampler(local)
+    sampler.start()
+    sampler.mark(True)
+    launches0 = moe.moe_launch_count()
+    ms = timed(lambda x: tier.forward(x, y=y), args.steps)
+    launches = moe.moe_launch_count() - launches0
+    sampler.mark(False)
+    clocks = sampler.stop()
+    if moe.moe_get_device_status(tier.ws) != moe.MOE_OK:
+        raise RuntimeError("device status not OK after the timed region")
+    s1 = tier.stats()
+    K = args.steps
+    d = {k: s1[k] - s0[k] for k in ("hits", "misses", "evictions", "extra_passes",
+                                    "bytes_loaded")}
+    loaded = d["bytes_loaded"] / K
+    bound_ms = resident_ms / K + loaded / (link * 1e9) * 1e3
+    value = cfg.T * K / (ms / 1e3)
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
+        "config": {"workload": cfg.name + "@tier%d" % args.tier_slots, "T": cfg.T, "d": cfg.d,
+                   "E": cfg.E, "I": cfg.I, "k": cfg.k, "shared": cfg.S,
+                   "expert_weights": "host memory, %d HBM slots of %d experts"
+                                     % (s1["n_slots"], cfg.E + cfg.S),
+                   "inputs": "%d token batches in rotation" % len(xs),
+                   "parallelism": "single GPU"},
+        "roofline": {"bound": "host link + resident layer", "achieved_ms": ms / K,
+                     "bound_ms": bound_ms, "frac": bound_ms / (ms / K),
+                     "host_link_gbs": link, "resident_ms_per_step": resident_ms / K,
+                     "h2d_bytes_per_step": loaded, "peak_source": "measured in this run"},
+        "tier": {"hit_rate": d["hits"] / max(1, d["hits"] + d["misses"]),
+                 "misses_per_step": d["misses"] / K, "evictions_per_step": d["evictions"] / K,
+                 "extra_passes_per_step": d["extra_passes"] / K,
+                 "h2d_gbs_achieved": d["bytes_loaded"] / (ms / 1e3) / 1e9},
+        "gpu_launches": launches,
+        "launch_mode": "direct (a host wait per step)",
+        "clocks": clocks,
+    }
+    tier.close()
+    return out
+
+
 # ---------------------------------------------------------------- the oracle (CPU)
 def _oracle_inputs(cfg, inp):
     return {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
@@ -454,6 +563,11 @@ def main():
                     help="expert weights in the layer's dtype, or Q8_0 blocks")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time direct launches instead of CUDA-graph replays")
+    ap.add_argument("--tier-slots", type=int, default=0,
+                    help="> 0: run the layer through the expert tier with this many HBM "
+                         "expert slots (experts in host memory)")
+    ap.add_argument("--tier-inputs", type=int, default=8,
+                    help="token batches in rotation for --tier-slots")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3  # the timing rules want at least three untimed steps
@@ -462,8 +576,12 @@ def main():
     if world > 1 and args.impl == "ours":
         torch.distributed.init_process_group("nccl")
     try:
-        out = run_reference(args, rank, world) if args.impl == "reference" else \
-            run_gpu(args, rank, world)
+        if args.impl == "reference":
+            out = run_reference(args, rank, world)
+        elif args.tier_slots > 0:
+            out = run_tier(args, rank, world) if rank == 0 else None
+        else:
+            out = run_gpu(args, rank, world)
         if out is not None:
             print(json.dumps(out), flush=True)
     finally:
