@@ -384,6 +384,20 @@ def host_link_gbs(dev, n_bytes=1 << 30, reps=3):
     return best
 
 
+def host_huge_fraction(nbytes):
+    """Share of nbytes that this process holds in transparent huge pages (Linux;
+    None elsewhere): the device reads host memory through its own address
+    translation, and base pages make scattered expert loads much slower."""
+    try:
+        with open("/proc/self/smaps_rollup") as f:
+            for line in f:
+                if line.startswith("AnonHugePages:"):
+                    return min(1.0, int(line.split()[1]) * 1024 / max(1, nbytes))
+    except OSError:
+        pass
+    return None
+
+
 def run_tier(args, rank, world):
     """The layer through the expert tier: expert projections in page-locked host
     memory, args.tier_slots expert slots in HBM.  Steps cycle through
@@ -402,9 +416,10 @@ def run_tier(args, rank, world):
     desc = moe.desc_from_config(cfg)
     host_w = []
     for n in ("Wg", "Wu", "Wd"):
-        h = torch.empty(inp[n].shape, dtype=inp[n].dtype, pin_memory=True)
+        h = moe.host_empty(inp[n].shape, inp[n].dtype)  # huge-page backed, page-locked
         h.copy_(inp[n])
         host_w.append(h)
+    huge = host_huge_fraction(sum(h.numel() * h.element_size() for h in host_w))
     expert_bytes = 3 * cfg.I * cfg.d * 2
     tier = moe.ExpertTier(desc, inp["Wr"], *host_w, args.tier_slots * expert_bytes,
                           logit_bias=inp["logit_bias"], sel_bias=inp["sel_bias"])
@@ -467,7 +482,8 @@ def run_tier(args, rank, world):
         "tier": {"hit_rate": d["hits"] / max(1, d["hits"] + d["misses"]),
                  "misses_per_step": d["misses"] / K, "evictions_per_step": d["evictions"] / K,
                  "extra_passes_per_step": d["extra_passes"] / K,
-                 "h2d_gbs_achieved": d["bytes_loaded"] / (ms / 1e3) / 1e9},
+                 "h2d_gbs_achieved": d["bytes_loaded"] / (ms / 1e3) / 1e9,
+                 "host_weights_in_huge_pages": huge},
         "gpu_launches": launches,
         "launch_mode": "direct (a host wait per step)",
         "clocks": clocks,

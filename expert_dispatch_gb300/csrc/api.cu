@@ -281,12 +281,20 @@ struct moe_expert_tier {
   int nE = 0, n_slots = 0;
   size_t mat_bytes = 0;  // one expert's Wg (= Wu = Wd) bytes
   const uint8_t* host[3] = {nullptr, nullptr, nullptr};
+  const void* host_dev[3] = {nullptr, nullptr, nullptr};  // device-visible addresses, or null
   bool registered[3] = {false, false, false};
   void* pool[3] = {nullptr, nullptr, nullptr};  // Wg, Wu, Wd slots
   int32_t* host_tab = nullptr;  // pinned: [nE + 1] batch bounds, then [nE][nE] pass tables
   int32_t* dev_tab = nullptr;   // [nE][nE] pass tables
   cudaEvent_t done = nullptr;
   bool done_recorded = false;
+  // Slot loads run on a stream of their own, joined to the caller's by
+  // events: large host -> device copies enqueued between kernels launched
+  // with programmatic dependent launch ran at a fraction of the link's
+  // bandwidth, and a load kernel there would be the programmatic predecessor
+  // of the FFN kernel that reads what it wrote.
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ready = nullptr, copied = nullptr;
   uint64_t bytes_loaded = 0;
   SlotCache cache;
   std::mutex mu;
@@ -307,10 +315,56 @@ void tier_free(moe_expert_tier* t) {
   }
   if (t->dev_tab) cudaFree(t->dev_tab);
   if (t->host_tab) cudaFreeHost(t->host_tab);
+  if (t->copy_stream) {
+    cudaStreamSynchronize(t->copy_stream);
+    cudaStreamDestroy(t->copy_stream);
+  }
+  if (t->ready) cudaEventDestroy(t->ready);
+  if (t->copied) cudaEventDestroy(t->copied);
   delete t;
 }
 
 // Copy expert e's three projections into `slot` (host -> device, on stream s).
+moe_status tier_load(moe_expert_tier* t, int e, int slot, cudaStream_t s);
+
+// Load the listed experts (load[i] set, of pass p unless pass is null) into
+// their slots on the tier's copy stream, after everything enqueued on s so far
+// (so no slot is overwritten while earlier kernels read it); work enqueued on
+// s afterwards waits for them.  One load kernel when the host arrays are
+// device-visible, else three copies per expert.
+moe_status tier_load_all(moe_expert_tier* t, const int32_t* experts, const int32_t* slot,
+                         const int32_t* load, const int32_t* pass, int n, int p,
+                         cudaStream_t s) {
+  ExpertLoadJobs jobs;
+  int n_jobs = 0;
+  for (int i = 0; i < n; ++i) {
+    if (!load[i] || (pass != nullptr && pass[i] != p)) continue;
+    if (experts[i] < 0 || experts[i] >= t->nE || slot[i] < 0 || slot[i] >= t->n_slots ||
+        n_jobs >= kMaxExpertLoadJobs)
+      return MOE_ERR_INVALID_ARG;
+    jobs.job[n_jobs++] = make_int2(experts[i], slot[i]);
+  }
+  if (n_jobs == 0) return MOE_OK;
+  if (cudaEventRecord(t->ready, s) != cudaSuccess ||
+      cudaStreamWaitEvent(t->copy_stream, t->ready, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (t->host_dev[0] && t->host_dev[1] && t->host_dev[2]) {
+    if (launch_load_experts(jobs, n_jobs, t->host_dev, t->pool, t->mat_bytes, t->copy_stream) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    t->bytes_loaded += (uint64_t)n_jobs * 3 * t->mat_bytes;
+  } else {
+    for (int j = 0; j < n_jobs; ++j) {
+      const moe_status st = tier_load(t, jobs.job[j].x, jobs.job[j].y, t->copy_stream);
+      if (st != MOE_OK) return st;
+    }
+  }
+  if (cudaEventRecord(t->copied, t->copy_stream) != cudaSuccess ||
+      cudaStreamWaitEvent(s, t->copied, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status tier_load(moe_expert_tier* t, int e, int slot, cudaStream_t s) {
   for (int i = 0; i < 3; ++i) {
     if (cudaMemcpyAsync(static_cast<uint8_t*>(t->pool[i]) + (size_t)slot * t->mat_bytes,
@@ -551,6 +605,14 @@ moe_status moe_tier_create(const moe_layer_desc* desc, const void* Wg_host, cons
       t->registered[i] = true;
     else
       (void)cudaGetLastError();
+    // the device-visible address of page-locked, mapped host memory (null
+    // when there is none: slot loads then use copies)
+    void* dp = nullptr;
+    if (cudaHostGetDevicePointer(&dp, const_cast<uint8_t*>(t->host[i]), 0) == cudaSuccess &&
+        (reinterpret_cast<uintptr_t>(dp) & 15u) == 0)
+      t->host_dev[i] = dp;
+    else
+      (void)cudaGetLastError();
     if (cudaMalloc(&t->pool[i], (size_t)n_slots * mat_bytes) != cudaSuccess) {
       (void)cudaGetLastError();
       tier_free(t);
@@ -561,7 +623,10 @@ moe_status moe_tier_create(const moe_layer_desc* desc, const void* Wg_host, cons
                     ((size_t)nE + 1 + (size_t)nE * nE) * 4, cudaHostAllocDefault) !=
           cudaSuccess ||
       cudaMalloc(reinterpret_cast<void**>(&t->dev_tab), (size_t)nE * nE * 4) != cudaSuccess ||
-      cudaEventCreateWithFlags(&t->done, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventCreateWithFlags(&t->done, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&t->ready, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&t->copied, cudaEventDisableTiming) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&t->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
     (void)cudaGetLastError();
     tier_free(t);
     return MOE_ERR_CUDA;
@@ -595,11 +660,9 @@ moe_status moe_tier_prefetch(moe_expert_tier* tier, const int32_t* experts, int 
     return MOE_ERR_INVALID_ARG;
   if (tier->done_recorded && cudaStreamWaitEvent(s, tier->done, 0) != cudaSuccess)
     return MOE_ERR_CUDA;
-  for (int i = 0; i < n; ++i) {
-    if (!load[i]) continue;
-    const moe_status st = tier_load(tier, experts[i], slot[i], s);
-    if (st != MOE_OK) return st;
-  }
+  const moe_status st =
+      tier_load_all(tier, experts, slot.data(), load.data(), nullptr, n, 0, s);
+  if (st != MOE_OK) return st;
   if (cudaEventRecord(tier->done, s) != cudaSuccess) return MOE_ERR_CUDA;
   tier->done_recorded = true;
   return MOE_OK;
@@ -662,9 +725,9 @@ moe_status moe_tier_forward(moe_expert_tier* tier, const moe_layer_desc* desc, c
     int32_t* dtab = tier->dev_tab + (size_t)p * nE;
     if (cudaMemcpyAsync(dtab, tab, (size_t)nE * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
       return MOE_ERR_CUDA;
-    for (int i = 0; i < n; ++i)
-      if (pass[i] == p && load[i] && (st = tier_load(tier, active[i], slot[i], s)) != MOE_OK)
-        return st;
+    if ((st = tier_load_all(tier, active.data(), slot.data(), load.data(), pass.data(), n, p,
+                            s)) != MOE_OK)
+      return st;
     if (launch_ffn_tc(W.x_perm, W.offsets, nE, P, desc->d, desc->I, mean_rows, tier->pool[0],
                       tier->pool[1], tier->pool[2], nullptr, W.h, W.y_perm, W.flags, s,
                       tier->n_slots, dtab) != cudaSuccess)

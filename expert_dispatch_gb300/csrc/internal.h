@@ -112,6 +112,16 @@ cudaError_t launch_scatter_rows(int dtype, bool to_f16, const void* x, const int
                                 const int32_t* total_rows, int T, int ks, int d, void* x_perm,
                                 int* flags, cudaStream_t s);
 
+// Expert loads of the host-memory tier (one launch, plain stream order): for
+// each job (expert, slot), its three projections of mat_bytes each from
+// host[0..2] (device-visible addresses of the host arrays) into pool[0..2].
+constexpr int kMaxExpertLoadJobs = 1028;
+struct ExpertLoadJobs {
+  int2 job[kMaxExpertLoadJobs];  // x: expert, y: slot
+};
+cudaError_t launch_load_experts(const ExpertLoadJobs& jobs, int n, const void* const host[3],
+                                void* const pool[3], size_t mat_bytes, cudaStream_t s);
+
 cudaError_t launch_gather_rows(int dtype, const void* x, const int32_t* tok_idx,
                                const int32_t* total_rows, int P, int T, int d, void* x_perm,
                                int* flags, cudaStream_t s);

@@ -156,6 +156,30 @@ __global__ void __launch_bounds__(kScatterThreads)
   if (TO_F16 && __syncthreads_or(overflow) && threadIdx.x == 0) flag_error(flags, kErrDeviceInput);
 }
 
+// Expert loads of the host-memory tier: job j moves expert jobs[j].x's three
+// projections (vec_per_mat 16-byte vectors each, from the host arrays mapped
+// into the device's address space) into slot jobs[j].y of the three pools.
+// SM loads over the host link keep their bandwidth for scattered experts,
+// where copy-engine transfers of the same blocks varied several-fold.
+__global__ void __launch_bounds__(512)
+    load_experts_kernel(const __grid_constant__ ExpertLoadJobs jobs, int n,
+                        const uint4* __restrict__ h0, const uint4* __restrict__ h1,
+                        const uint4* __restrict__ h2, uint4* __restrict__ p0,
+                        uint4* __restrict__ p1, uint4* __restrict__ p2, size_t vec_per_mat) {
+  const size_t per_job = 3 * vec_per_mat;
+  const size_t total = per_job * (size_t)n;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += stride) {
+    const size_t j = i / per_job, r = i - j * per_job;
+    const int p = (int)(r / vec_per_mat);
+    const size_t o = r - (size_t)p * vec_per_mat;
+    const int2 job = jobs.job[j];
+    const uint4* src = p == 0 ? h0 : p == 1 ? h1 : h2;
+    uint4* dst = p == 0 ? p0 : p == 1 ? p1 : p2;
+    dst[(size_t)job.y * vec_per_mat + o] = ld_stream(src + (size_t)job.x * vec_per_mat + o);
+  }
+}
+
 __device__ __forceinline__ void add8(float (&acc)[8], uint4 v, float w) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
 #pragma unroll
@@ -331,6 +355,18 @@ cudaError_t launch_gather_rows_to_f16(const void* x, const int32_t* tok_idx,
   (void)launch_kernel(gather_rows_to_f16_kernel, (P + 7) / 8, 256, 0, s,
                       static_cast<const uint4*>(x), tok_idx, total_rows, P, T, d / 8,
                       static_cast<uint4*>(x_perm), flags);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_load_experts(const ExpertLoadJobs& jobs, int n, const void* const host[3],
+                                void* const pool[3], size_t mat_bytes, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (n > kMaxExpertLoadJobs || mat_bytes % 16) return cudaErrorInvalidValue;
+  count_launch();
+  load_experts_kernel<<<num_sms() * 4, 512, 0, s>>>(
+      jobs, n, static_cast<const uint4*>(host[0]), static_cast<const uint4*>(host[1]),
+      static_cast<const uint4*>(host[2]), static_cast<uint4*>(pool[0]),
+      static_cast<uint4*>(pool[1]), static_cast<uint4*>(pool[2]), mat_bytes / 16);
   return cudaGetLastError();
 }
 

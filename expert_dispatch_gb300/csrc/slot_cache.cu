@@ -17,11 +17,21 @@
 // another in stream order, so a slot is overwritten only after the previous
 // pass's kernels have read it).  Pins last for one assignment; ordering
 // against earlier device work is the caller's stream order.
+//
+// moe_host_alloc / moe_host_free (the tier's host memory) are here too.
 #include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+#include <sys/mman.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <thread>
 #include <vector>
+
+#include <cuda_runtime.h>
 
 #include "../../include/moe.h"
 #include "internal.h"
@@ -113,6 +123,29 @@ void SlotCache::fill_stats(moe_tier_stats* out) const {
 
 }  // namespace moe
 
+namespace {
+
+// Host memory for the tier's colder level.  The device reads host memory
+// through its own address translation, and with base pages (64 KB on this
+// class of host) a region of tens of GB misses that translation often enough
+// to halve host -> device copy bandwidth on first touch; memory backed by
+// transparent huge pages does not.  So: align to the huge-page size, ask for
+// huge pages, fault every page in (in parallel), then page-lock it.
+size_t huge_page_bytes() {
+  size_t v = 0;
+  if (FILE* f = fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+    unsigned long long x = 0;
+    if (fscanf(f, "%llu", &x) == 1) v = (size_t)x;
+    fclose(f);
+  }
+  return v >= 4096 && (v & (v - 1)) == 0 ? v : (size_t)2 << 20;
+}
+
+std::mutex g_host_mu;
+std::map<void*, size_t> g_host_blocks;
+
+}  // namespace
+
 struct moe_slot_cache {
   moe::SlotCache cache;
   std::mutex mu;
@@ -153,6 +186,49 @@ moe_status moe_slot_cache_get_stats(moe_slot_cache* c, moe_tier_stats* out) {
   std::lock_guard<std::mutex> g(c->mu);
   c->cache.fill_stats(out);
   return MOE_OK;
+}
+
+moe_status moe_host_alloc(size_t bytes, void** out) {
+  if (!out || bytes == 0) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  const size_t align = huge_page_bytes();
+  const size_t size = (bytes + align - 1) / align * align;
+  void* p = aligned_alloc(align, size);
+  if (!p) return MOE_ERR_CUDA;
+  (void)madvise(p, size, MADV_HUGEPAGE);  // advice only: base pages still work
+  const unsigned hw = std::thread::hardware_concurrency();
+  const size_t n_threads = std::min<size_t>(hw ? hw : 1, std::max<size_t>(1, size / align));
+  std::vector<std::thread> pool;
+  const size_t per = (size / n_threads + align - 1) / align * align;
+  for (size_t i = 0; i < n_threads; ++i) {
+    const size_t lo = i * per;
+    if (lo >= size) break;
+    const size_t len = std::min(per, size - lo);
+    pool.emplace_back([p, lo, len] { memset(static_cast<char*>(p) + lo, 0, len); });
+  }
+  for (auto& t : pool) t.join();
+  if (cudaHostRegister(p, size, cudaHostRegisterDefault) != cudaSuccess) {
+    (void)cudaGetLastError();
+    free(p);
+    return MOE_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> g(g_host_mu);
+  g_host_blocks[p] = size;
+  *out = p;
+  return MOE_OK;
+}
+
+moe_status moe_host_free(void* p) {
+  if (!p) return MOE_OK;
+  {
+    std::lock_guard<std::mutex> g(g_host_mu);
+    auto it = g_host_blocks.find(p);
+    if (it == g_host_blocks.end()) return MOE_ERR_INVALID_ARG;
+    g_host_blocks.erase(it);
+  }
+  const cudaError_t e = cudaHostUnregister(p);
+  free(p);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -42,7 +42,8 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_d
             "moe_expert_ffn_q8", "moe_layer_forward_q8", "moe_slot_cache_create",
             "moe_slot_cache_destroy", "moe_slot_cache_assign", "moe_slot_cache_slot_of",
             "moe_slot_cache_get_stats", "moe_tier_create", "moe_tier_destroy",
-            "moe_tier_prefetch", "moe_tier_forward", "moe_tier_get_stats")
+            "moe_tier_prefetch", "moe_tier_forward", "moe_tier_get_stats", "moe_host_alloc",
+            "moe_host_free")
 
 
 class MoeError(RuntimeError):
@@ -132,6 +133,8 @@ def lib():
     L.moe_tier_prefetch.argtypes = [vp, vp, i32, vp]
     L.moe_tier_forward.argtypes = [vp, D, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_tier_get_stats.argtypes = [vp, TS]
+    L.moe_host_alloc.argtypes = [sz, vpp]
+    L.moe_host_free.argtypes = [vp]
     L.moe_profile_enable.argtypes = [i32]
     L.moe_profile_query.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
                                     ctypes.POINTER(ctypes.c_float)]
@@ -473,6 +476,35 @@ class SlotCache:
         _check(lib().moe_slot_cache_get_stats(self._h, ctypes.byref(st)),
                "moe_slot_cache_get_stats")
         return st.as_dict()
+
+
+class _HostBlock:
+    """Owner of one moe_host_alloc block; frees it when the last view is gone."""
+
+    def __init__(self, nbytes):
+        p = ctypes.c_void_p()
+        _check(lib().moe_host_alloc(nbytes, ctypes.byref(p)), "moe_host_alloc")
+        self.ptr, self.nbytes = p.value, nbytes
+
+    def __del__(self):
+        if getattr(self, "ptr", None):
+            lib().moe_host_free(ctypes.c_void_p(self.ptr))
+            self.ptr = None
+
+
+def host_empty(shape, dtype=torch.bfloat16) -> torch.Tensor:
+    """A CPU tensor in moe_host_alloc memory (page-locked, huge-page backed, zeroed):
+    the fast home for an expert tier's projections."""
+    import numpy as np
+    n = 1
+    for v in shape:
+        n *= int(v)
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    block = _HostBlock(max(nbytes, 1))
+    buf = (ctypes.c_uint8 * nbytes).from_address(block.ptr)
+    buf._owner = block  # tensor -> numpy array -> this buffer -> the block
+    arr = np.frombuffer(buf, dtype=np.uint8)
+    return torch.from_numpy(arr).view(dtype).view(*shape)
 
 
 def _host_p(t, dtype, what):

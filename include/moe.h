@@ -299,11 +299,22 @@ moe_status moe_slot_cache_assign(moe_slot_cache* cache, const int32_t* experts, 
 moe_status moe_slot_cache_slot_of(moe_slot_cache* cache, int expert, int32_t* slot);
 moe_status moe_slot_cache_get_stats(moe_slot_cache* cache, moe_tier_stats* out);
 
+/* Host memory for the tier's expert projections: page-locked, aligned to the
+   host's transparent-huge-page size and backed by huge pages where the host
+   allows it (zero-filled).  Host -> device copies from such memory keep the
+   link's bandwidth even on first touch of a large region; copies from
+   base-page memory can run at half of it.  Free with moe_host_free (which
+   rejects pointers it did not hand out).  Host only; MOE_ERR_CUDA when the
+   allocation or page-locking fails. */
+moe_status moe_host_alloc(size_t bytes, void** out);
+moe_status moe_host_free(void* ptr);
+
 /* The expert tier.  moe_tier_create keeps pointers to the layer's expert
    projections in HOST memory (bf16, layouts as in moe_layer_forward:
    Wg/Wu [E+S, I, d], Wd [E+S, d, I]); the caller keeps them alive and
-   unchanged until moe_tier_destroy.  The tier page-locks them if they are
-   not already (and unlocks what it locked on destroy), and allocates
+   unchanged until moe_tier_destroy (moe_host_alloc memory is the fast
+   choice).  The tier page-locks them if they are not already (and unlocks
+   what it locked on destroy), and allocates
    n_slots = min(E+S, floor(hbm_budget_bytes / (6 I d))) expert slots in
    HBM on the current device (MOE_ERR_INVALID_ARG below one slot).  desc
    fixes d, E, k, I, S, gate and dtype (MOE_BF16 only; other dtypes are
@@ -313,12 +324,13 @@ moe_status moe_slot_cache_get_stats(moe_slot_cache* cache, moe_tier_stats* out);
    this call's T: route and plan on the device; the routing decision (the
    expert batch sizes) is copied to the host, which WAITS for the stream
    once; slots are assigned (moe_slot_cache_assign), the missing experts
-   are copied into their slots on `stream`, and the FFN runs once per pass
+   are copied into their slots (on a copy stream of the tier's, ordered
+   after the work already on `stream`), and the FFN runs once per pass
    over the experts of that pass; then the combine.  The result equals
    moe_layer_forward's bit for bit.  Calls on one tier are serialized
    (the tier orders its work after its previous call's, whatever stream).
    moe_tier_prefetch brings up to n_slots of the listed experts in ahead of
-   use (a caller-supplied hotlist), asynchronously on `stream`.
+   use (a caller-supplied hotlist), asynchronously, ordered after `stream`.
    moe_tier_destroy waits for the tier's outstanding work. */
 typedef struct moe_expert_tier moe_expert_tier;
 moe_status moe_tier_create(const moe_layer_desc* desc, const void* Wg_host, const void* Wu_host,

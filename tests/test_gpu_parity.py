@@ -218,7 +218,11 @@ def test_expert_ffn_and_combine_parity(cfg):
 
 
 # ---------------------------------------------------------------- whole layer, small
-LAYER_CASES = FFN_CASES + [ROUTER_CASES[2], ROUTER_CASES[3]]
+# the largest shape the layer record admits: E=1024 routed + 4 shared experts
+# (1028 groups, the grouped GEMM's limit), top-32; softmax scores, whose gaps
+# among the top 33 of 1024 stay wide enough for the routing margin
+MAX_GROUPS = LayerConfig("l_max_groups", T=40, d=128, E=1024, I=64, k=32, S=4, norm_topk=1)
+LAYER_CASES = FFN_CASES + [ROUTER_CASES[2], ROUTER_CASES[3], MAX_GROUPS]
 
 
 @pytest.mark.parametrize("cfg", LAYER_CASES, ids=lambda c: c.name)
@@ -237,6 +241,19 @@ def test_layer_forward_parity_small(cfg):
     moe_part = host(y).double().numpy() - host(residual).double().numpy()
     moe_ref = y_ref - host(residual).double().numpy()
     assert rel_err(moe_part, moe_ref) <= y_tol(cfg), rel_err(moe_part, moe_ref)
+
+
+def test_layer_forward_with_no_tokens_is_a_no_op():
+    cfg = FFN_CASES[4]
+    inp = _case(cfg, seed=2)
+    desc = moe.desc_from_config(cfg, T=0)
+    ws = torch.zeros((16,), dtype=torch.uint8, device=DEV)
+    y = torch.full((1, cfg.d), 7.0, dtype=torch.float32, device=DEV)
+    c0 = moe.moe_launch_count()
+    moe.moe_layer_forward(desc, inp["x"][:0], inp["Wr"], inp["logit_bias"], inp["sel_bias"],
+                          inp["Wg"], inp["Wu"], inp["Wd"], None, y[:0], None, None, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_launch_count() == c0 and bool((y == 7.0).all())
 
 
 def test_layer_forward_is_deterministic():

@@ -30,7 +30,7 @@ def _cuda():
 def _host_weights(inp):
     out = []
     for n in ("Wg", "Wu", "Wd"):
-        h = torch.empty(inp[n].shape, dtype=inp[n].dtype, pin_memory=True)
+        h = moe.host_empty(inp[n].shape, inp[n].dtype)
         h.copy_(inp[n])
         out.append(h)
     return tuple(out)
@@ -109,6 +109,17 @@ def test_prefetch_makes_the_next_step_hit():
     s1 = tier.stats()
     assert s1["misses"] == s0["misses"] and s1["hits"] == len(needed)
     tier.close()
+
+
+def test_host_memory_for_the_tier():
+    h = moe.host_empty((3, 5, 64), torch.bfloat16)
+    assert h.device.type == "cpu" and h.is_contiguous() and bool((h == 0).all())
+    v = h[1]
+    del h
+    v.fill_(2.0)  # the block outlives the tensor it was made for while a view exists
+    assert bool((v == 2.0).all())
+    with pytest.raises(moe.MoeError):
+        moe._check(moe.lib().moe_host_free(moe.ctypes.c_void_p(12345)), "moe_host_free")
 
 
 def test_tier_rejects_bad_arguments():
