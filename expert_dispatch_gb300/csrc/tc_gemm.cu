@@ -331,12 +331,12 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
   if (P == 0) return cudaSuccess;
   const uint64_t cap = (uint64_t)tc_row_capacity(P);
   // Token tiles by mean batch size: 32 rows for decode-sized batches (deep
-  // pipelines).  Above that, gate/up uses 128 rows while batches are a few
-  // hundred rows (its two accumulators then fit twice in TMEM, so the epilogue
-  // overlaps the next unit's MMAs) and 256 rows for larger batches (tensor
-  // bound: the largest MMA); down uses 256 rows (fewest weight passes).
+  // pipelines); 160 rows while batches are up to a few hundred rows (a batch
+  // of 95-160 rows is one tile, so its weights pass once, with room for 4-6
+  // stages); 256 rows for larger batches (tensor bound: the largest MMA).
   const bool small = mean_rows <= 48.0;
-  const int bn = small ? 32 : mean_rows <= 256.0 ? 128 : 256;
+  const int bn = small ? 32 : mean_rows <= 256.0 ? 160 : 256;
+  const int bn2 = bn;
   // token operands: 32-row boxes for partial tiles, tile-high boxes for full ones
   CUtensorMap tg, tu, tx, txf, td, th, thf, thf2;
   if (n_mats <= 0) n_mats = n_groups;
@@ -344,22 +344,22 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
       !make_tmap(&tu, Wu, d, (uint64_t)n_mats * I, 128) ||
       !make_tmap(&tx, x_perm, d, cap, 32) || !make_tmap(&txf, x_perm, d, cap, bn) ||
       !make_tmap(&td, Wd, I, (uint64_t)n_mats * d, 128) || !make_tmap(&th, h, I, cap, 32) ||
-      !make_tmap(&thf, h, I, cap, 32) || !make_tmap(&thf2, h, I, cap, 256))
+      !make_tmap(&thf, h, I, cap, 32) || !make_tmap(&thf2, h, I, cap, bn2))
     return cudaErrorInvalidValue;
   Params p1{offsets, n_groups, 0, I, d, h, I, nullptr, err, P, 0, 0, group_slot};
   const long long u1 = (long long)((I + 127) / 128) * ((P + bn - 1) / bn + n_groups);
   cudaError_t e;
   if (small)
     e = launch_tc<MODE_GATEUP, 32, 6>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
-  else if (bn == 128)
-    e = launch_tc<MODE_GATEUP, 128, 4>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
+  else if (bn == 160)
+    e = launch_tc<MODE_GATEUP, 160, 4>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
   else
     e = launch_tc<MODE_GATEUP, 256, 3>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
   if (e != cudaSuccess) return e;
-  const int bn2 = small ? 32 : 256;
   Params p2{offsets, n_groups, 0, d, I, y_perm, d, slot_w, err, P, 0, 0, group_slot};
   const long long u2 = (long long)((d + 127) / 128) * ((P + bn2 - 1) / bn2 + n_groups);
   if (small) return launch_tc<MODE_DOWN, 32, 10>(td, td, th, thf, p2, u2, "ffn_down_tc", s);
+  if (bn2 == 160) return launch_tc<MODE_DOWN, 160, 6>(td, td, th, thf2, p2, u2, "ffn_down_tc", s);
   return launch_tc<MODE_DOWN, 256, 4>(td, td, th, thf2, p2, u2, "ffn_down_tc", s);
 }
 
