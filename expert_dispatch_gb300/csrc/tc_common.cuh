@@ -178,9 +178,10 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, i
 // For the last two the whole unit is first turned into packed 16-bit pairs
 // held in registers; the TMEM buffer is handed back before the global
 // stores, so those overlap the next unit's MMAs instead of delaying them.
-// With NPART = 2 the unit's K blocks were accumulated into two partial sets
-// (even and odd K blocks of the unit, NACC * BN columns apart), added here
-// in that order; a unit with a single K block has only the first.
+// With NPART > 1 the unit's K blocks were accumulated into NPART partial
+// sets (K block j of the unit into set j % NPART, NACC * BN columns apart),
+// added here in set order; a unit with fewer K blocks than sets has only
+// the first ones.
 template <int MODE, int BN, int NACC, int NBUF, bool H_F16 = false, int NPART = 1>
 __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_tiles, int KB,
                                               const int* prefix, const int* gstart,
@@ -202,15 +203,16 @@ __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_
     const bool mvalid = m < p.Mg;
     const uint32_t tb =
         tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NPART * NACC * BN);
-    const bool two = NPART == 2 && t.kb1 - t.kb0 >= 2;
+    const int nparts = NPART == 1 ? 1 : min(NPART, t.kb1 - t.kb0);
     // accumulator columns c0 .. c0 + 15 (both operands, partial sets added)
     auto load16 = [&](int c0, uint32_t (&a)[16], uint32_t (&b)[16]) {
       tmem_ld16(tb + c0, a);
       if (NACC == 2) tmem_ld16(tb + BN + c0, b);
-      if (two) {
+      for (int pp = 1; pp < nparts; ++pp) {
         uint32_t a2[16], b2[16];
-        tmem_ld16(tb + NACC * BN + c0, a2);
-        if (NACC == 2) tmem_ld16(tb + NACC * BN + BN + c0, b2);
+        const uint32_t tp = tb + (uint32_t)(pp * NACC * BN);
+        tmem_ld16(tp + c0, a2);
+        if (NACC == 2) tmem_ld16(tp + BN + c0, b2);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {

@@ -20,9 +20,11 @@
 //   * the MMA issuer (kind::f16, fp16 operands, fp32 accumulation) consumes a
 //     converted stage and a token stage and releases both with
 //     tcgen05.commit.  With 32-token tiles an MMA is so short that a single
-//     issuing thread cannot keep up with the weight stream, so NI = 2 issuers
-//     split each unit's K blocks by parity into two partial accumulators,
-//     which the epilogue adds.
+//     issuing thread cannot keep up with the weight stream (one thread
+//     issues at most one MMA per ~45 cycles, and each K block also costs it
+//     two waits, a fence and two commits), so NI issuers (2 for gate/up, 4
+//     for down) take K block j of each unit when j % NI is theirs, into NI
+//     partial accumulators that the epilogue adds.
 // A weight stage is thus held only from its TMA to the converters' loads,
 // so the in-flight depth of the weight stream does not shrink by the decode
 // and MMA latency; the weight loader never waits for the predecessor grid
@@ -53,7 +55,7 @@ using tc::Unit;
 constexpr int kConvWarps = 8;
 constexpr int kFirstEpiWarp = 3;  // warps 0-2: weight loader, MMA issuer, token loader
 constexpr int kFirstConvWarp = kFirstEpiWarp + tc::kEpiWarps;
-constexpr int kIssuer2 = kFirstConvWarp + kConvWarps;  // second MMA issuer (NI = 2)
+constexpr int kIssuer2 = kFirstConvWarp + kConvWarps;  // issuers 2 .. NI: warps kIssuer2 ..
 constexpr int threads_q8(int NI) { return 32 * (kIssuer2 + NI - 1); }
 
 template <int MODE, int BN, int WS, int TS, int CS, int NI>
@@ -67,6 +69,10 @@ struct CfgQ8 {
   static constexpr int B_BYTES = BN * 128;                // token rows of one K block
   static constexpr int T_OFF = WS * W_BYTES;
   static constexpr int NACC = NA;
+  // converter warps per K block: gate/up needs all of them (two operands x
+  // four lane quarters); down's single operand takes four, so two groups of
+  // four convert alternate K blocks concurrently
+  static constexpr int CONV_PER_BLOCK = NA == 2 ? kConvWarps : kConvWarps / 2;
   static constexpr int A_COLS = NA * 32 * CS;             // TMEM columns of the converted ring
   static constexpr int NBUF = 2 * NI * NACC * BN + A_COLS <= 512 ? 2 : 1;
   static constexpr int ACC_COLS = NBUF * NI * NACC * BN;  // [buffer][issuer][operand][BN]
@@ -82,7 +88,7 @@ struct CfgQ8 {
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "token tile");
   static_assert(COLS <= 512, "TMEM columns");
   static_assert(WS <= 32 && TS <= 32, "stages in flight tracked in 32-bit masks");
-  static_assert(NI == 1 || NI == 2, "issuers");
+  static_assert(NI >= 1 && NI <= 4, "issuers");
   static_assert(SMEM_TOTAL <= 232448, "shared memory");
 };
 
@@ -142,14 +148,14 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < WS; ++s) {
       mbar_init(w_full(s), 1);
-      mbar_init(w_empty(s), kConvWarps);
+      mbar_init(w_empty(s), C::CONV_PER_BLOCK);
     }
     for (int s = 0; s < TS; ++s) {
       mbar_init(t_full(s), 1);
       mbar_init(t_empty(s), 1);
     }
     for (int s = 0; s < CS; ++s) {
-      mbar_init(conv_full(s), kConvWarps);
+      mbar_init(conv_full(s), C::CONV_PER_BLOCK);
       mbar_init(conv_empty(s), 1);
     }
     for (int b = 0; b < C::NBUF; ++b) {
@@ -252,12 +258,12 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
       for (int s = 0; s < TS; ++s)
         if (armed & (1u << s)) tc::mbar_wait_drain(t_full(s), (armed_parity >> s) & 1u, p.err);
     }
-  } else if (warp == 1 || warp == kIssuer2) {
+  } else if (warp == 1 || warp >= kIssuer2) {
     // ------------------------------------------------------------ MMA issuer(s)
     // Issuer i takes the K blocks kb of each unit with (kb - kb0) % NI == i
     // into its own partial accumulators; every issuer commits each unit's
     // accumulators (accf counts NI arrivals) and the final drain.
-    const int me = warp == 1 ? 0 : 1;
+    const int me = warp == 1 ? 0 : warp - kIssuer2 + 1;
     if (lane == 0 && me < NI) {
       int it = 0;
       uint32_t kcount = 0;  // K blocks seen so far (indexes the token and converted rings)
@@ -310,15 +316,19 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
   } else {
     // ------------------------------------------------------------ converters
     // Warp w may write only TMEM lanes 32 (w % 4) .. +31, so thread (w, lane)
-    // owns weight row r = 32 (w % 4) + lane.  Gate/up: the first four
-    // converter warps decode operand 0, the other four operand 1, 64 weights
-    // per row; down: the two warps of a lane quarter take the two 32-weight
-    // halves of the K block.
-    constexpr int NCH = C::NA == 2 ? 4 : 2;  // 16-byte code chunks per thread
+    // owns weight row r = 32 (w % 4) + lane and decodes its 64 weights of a
+    // K block.  Gate/up: the first four converter warps decode operand 0,
+    // the other four operand 1.  Down: the first four take the even K blocks
+    // of this CTA's sequence, the other four the odd ones, so two K blocks
+    // are in conversion at once (a down K block is half the bytes of a
+    // gate/up one, and one at a time left the converters short of the
+    // weight stream).
+    constexpr int NCH = 4;  // 16-byte code chunks per thread: a 64-weight row
     const int cw = warp - kFirstConvWarp;
     const int q = warp & 3, r = q * 32 + lane;
     const int op = C::NA == 2 ? cw >> 2 : 0;
-    const int j0 = C::NA == 2 ? 0 : 2 * (cw >> 2);  // first chunk of this thread
+    const uint32_t group = C::NA == 2 ? 0u : (uint32_t)(cw >> 2);  // down: K-block parity
+    const int j0 = 0;
     const int swz = (r >> 1) & 3;
     const int code_off = op * C::QA_BYTES + r * 64;
     const int scale_off = C::SA_OFF + op * C::SA_BYTES + r * 2;  // + scale block * 256
@@ -329,6 +339,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit t = tc::decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
       for (int kb = t.kb0; kb < t.kb1; ++kb, ++kcount) {
+        if (C::NA == 1 && (kcount & 1u) != group) continue;
         const int ws = kcount % WS, cs = kcount % CS;
         if (!tc::mbar_wait_warp(w_full(ws), (kcount / WS) & 1u, abort_flag, p.err)) {
           ok = false;
@@ -365,11 +376,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
           o[8 * i + 6] = hi.z;
           o[8 * i + 7] = hi.w;
         }
-        const uint32_t dst = t_row + (uint32_t)(cs * C::NA * 32);
-        if constexpr (NCH == 4)
-          tmem_st32(dst, o);
-        else
-          tmem_st16(dst, o);
+        tmem_st32(t_row + (uint32_t)(cs * C::NA * 32), o);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -456,7 +463,7 @@ cudaError_t launch_ffn_tc_q8(const void* x_perm, const int32_t* offsets, int n_g
   Params p2{offsets, n_groups, 0, d, I, y_perm, d, slot_w, err, P};
   const long long u2 = (long long)((d + 127) / 128) * ((P + bn2 - 1) / bn2 + n_groups);
   const char* n2 = "ffn_down_tc_q8";
-  return small ? launch_q8<MODE_DOWN, 32, 18, 8, 8, 2>(qd, qd, sd, sd, th, th, p2, u2, n2, s)
+  return small ? launch_q8<MODE_DOWN, 32, 18, 8, 8, 4>(qd, qd, sd, sd, th, th, p2, u2, n2, s)
                : launch_q8<MODE_DOWN, 256, 12, 3, 8, 1>(qd, qd, sd, sd, th, thf2, p2, u2, n2, s);
 }
 
