@@ -741,6 +741,15 @@ moe_status moe_tier_forward(moe_expert_tier* tier, const moe_layer_desc* desc, c
   return MOE_OK;
 }
 
+moe_status moe_check_bounded_wait(void* workspace, size_t ws_bytes, int which, void* stream) {
+  if (!workspace || ws_bytes < 16 || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  if (which < 0 || which > 3) return MOE_ERR_INVALID_ARG;
+  return launch_bounded_wait_check(which, static_cast<int*>(workspace),
+                                   static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 moe_status moe_get_device_status(void* workspace, size_t ws_bytes, int clear, void* stream) {
   if (!workspace || ws_bytes < 16 || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -91,6 +91,10 @@ cudaError_t launch_router_logits_splitk(int dtype, const void* x, const void* Wr
 cudaError_t launch_router_logits_tc(const void* x, const void* Wr, int T, int d, int E,
                                     int ksplit, int kb_per, float* partial, int* err,
                                     cudaStream_t s);
+// One CTA waits on an mbarrier that nothing completes, with the bounded wait
+// named by `which` (0 thread, 1 warp, 2 wind-down, 3 two waits sharing an
+// abort flag); the wait expires and records kErrTimeout in *err.
+cudaError_t launch_bounded_wait_check(int which, int* err, cudaStream_t s);
 // per-token top-k and gate weights from the partial logits
 cudaError_t launch_router_topk(const float* partial, int ksplit, const float* logit_bias,
                                const float* sel_bias, int T, int E, int k, int gate,

@@ -377,4 +377,45 @@ cudaError_t launch_router_logits_tc(const void* x, const void* Wr, int T, int d,
   return launch_tc<MODE_ROUTER, 128, 6>(ta, ta, tb, tb128, p, units, "router_logits_tc", s);
 }
 
+// Self-check of the bounded waits that every tcgen05 kernel here uses: one CTA
+// waits on an mbarrier whose phase nothing completes.  The wait has to give up
+// after kWaitLimitNs, record kErrTimeout in *err and return, and the kernel
+// then ends normally, so the context stays usable.
+//   which 0: the single-thread wait (mbar_wait)
+//   which 1: the warp-uniform wait (mbar_wait_warp)
+//   which 2: the wind-down wait that ignores the abort flag (mbar_wait_drain)
+//   which 3: a warp-uniform wait and a single-thread wait sharing one abort
+//            flag: whichever expires first has to release the other
+__global__ void __launch_bounds__(64, 1) bounded_wait_check_kernel(int which, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const uint32_t b = smem_u32(&bar);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (which == 0) {
+    if (threadIdx.x == 0) mbar_wait(b, 0, &abort_flag, err);
+  } else if (which == 1) {
+    if (warp == 0) tc::mbar_wait_warp(b, 0, &abort_flag, err);
+  } else if (which == 2) {
+    if (threadIdx.x == 0) tc::mbar_wait_drain(b, 0, err);
+  } else {
+    if (warp == 0) tc::mbar_wait_warp(b, 0, &abort_flag, err);
+    else if (lane == 0) mbar_wait(b, 0, &abort_flag, err);
+  }
+  __syncthreads();
+}
+
+cudaError_t launch_bounded_wait_check(int which, int* err, cudaStream_t s) {
+  if (which < 0 || which > 3) return cudaErrorInvalidValue;
+  ProfScope pr("bounded_wait_check", s);
+  count_launch();
+  bounded_wait_check_kernel<<<1, 64, 0, s>>>(which, err);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -43,7 +43,7 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_d
             "moe_slot_cache_destroy", "moe_slot_cache_assign", "moe_slot_cache_slot_of",
             "moe_slot_cache_get_stats", "moe_tier_create", "moe_tier_destroy",
             "moe_tier_prefetch", "moe_tier_forward", "moe_tier_get_stats", "moe_host_alloc",
-            "moe_host_free")
+            "moe_host_free", "moe_check_bounded_wait")
 
 
 class MoeError(RuntimeError):
@@ -110,6 +110,7 @@ def lib():
     L.moe_combine.argtypes = [D, vp, vp, vp, vp, vp, vp]
     L.moe_layer_forward.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_get_device_status.argtypes = [vp, sz, i32, vp]
+    L.moe_check_bounded_wait.argtypes = [vp, sz, i32, vp]
     L.moe_status_string.argtypes = [i32]
     L.moe_status_string.restype = ctypes.c_char_p
     L.moe_launch_count.argtypes = []
@@ -417,6 +418,13 @@ def moe_get_device_status(ws, clear=False, stream=None) -> int:
     """Synchronizes the stream and returns the workspace's sticky device status."""
     return lib().moe_get_device_status(_p(ws, torch.uint8, "workspace"), ws.numel(),
                                        1 if clear else 0, _stream(stream))
+
+
+def moe_check_bounded_wait(ws, which, stream=None):
+    """Enqueues the bounded-wait self-check (see include/moe.h); afterwards
+    moe_get_device_status(ws) reports MOE_ERR_TIMEOUT."""
+    _check(lib().moe_check_bounded_wait(_p(ws, torch.uint8, "workspace"), ws.numel(), which,
+                                        _stream(stream)), "moe_check_bounded_wait")
 
 
 def moe_launch_count() -> int:

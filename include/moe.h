@@ -348,6 +348,19 @@ moe_status moe_tier_get_stats(moe_expert_tier* tier, moe_tier_stats* out);
    the copy itself fails).  clear != 0 resets the flag afterwards.          */
 moe_status moe_get_device_status(void* workspace, size_t ws_bytes, int clear, void* stream);
 
+/* Failure-detection self-check (no counterpart in the pages: it exercises the
+   library's own error path).  Enqueues on `stream` one small kernel that
+   waits on an mbarrier whose phase nothing completes, using the bounded wait
+   named by `which`: 0 the single-thread wait, 1 the warp-wide wait, 2 the
+   wind-down wait, 3 a warp-wide and a single-thread wait sharing one abort
+   flag.  The wait expires after about one second, sets the timeout bit of the
+   workspace's device flag and the kernel ends normally, so the CUDA context
+   stays usable; moe_get_device_status() then reports MOE_ERR_TIMEOUT.
+   Returns MOE_ERR_WORKSPACE for a missing, short (< 16 bytes) or unaligned
+   workspace, MOE_ERR_INVALID_ARG for another `which`, MOE_ERR_CUDA if the
+   launch fails, else MOE_OK. */
+moe_status moe_check_bounded_wait(void* workspace, size_t ws_bytes, int which, void* stream);
+
 /* Human-readable name of a status; never NULL. */
 const char* moe_status_string(moe_status status);
 
