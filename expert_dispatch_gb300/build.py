@@ -19,7 +19,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe.so")
 SOURCES = ["api.cu", "simt.cu", "plan.cu", "rows.cu", "tc_gemm.cu", "tc_gemm_q8.cu", "quant.cu",
-           "ffn_noalloc.cu", "slot_cache.cu"]
+           "ffn_noalloc.cu", "slot_cache.cu", "tc_gemm_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

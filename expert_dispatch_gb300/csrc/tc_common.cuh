@@ -182,24 +182,36 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, i
 // sets (K block j of the unit into set j % NPART, NACC * BN columns apart),
 // added here in set order; a unit with fewer K blocks than sets has only
 // the first ones.
-template <int MODE, int BN, int NACC, int NBUF, bool H_F16 = false, int NPART = 1>
+//
+// Units u0, u0 + ustride, ... are this CTA's; a unit's weight block covers
+// rows mt * MT + row_off .. + 127 of the group.  With PAIR the accumulator
+// buffers are released on the even CTA of the cluster (the pair's MMA
+// issuer), whatever CTA this is.
+template <int MODE, int BN, int NACC, int NBUF, bool H_F16 = false, int NPART = 1, int MT = 128,
+          bool PAIR = false>
 __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_tiles, int KB,
                                               const int* prefix, const int* gstart,
                                               uint32_t tmem_base, uint32_t accf0,
                                               uint32_t acce0, volatile int* abort_flag,
-                                              int first_warp) {
+                                              int first_warp, int u0, int ustride, int row_off) {
   constexpr int NCH = BN / 32;  // 16-column chunks per thread
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3;                   // TMEM lane quarter this warp may access
   const int half = (warp - first_warp) / 4;  // alternate 16-column chunks
+  auto release = [&](int buf) {  // lane 0: the accumulator buffer may be overwritten
+    if (PAIR)
+      mbar_arrive_cluster(mapa_shared(acce0 + 8u * buf, 0));
+    else
+      mbar_arrive(acce0 + 8u * buf);
+  };
   int it = 0;
-  for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+  for (int u = u0; u < total; u += ustride, ++it) {
     const Unit t = decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
     const int buf = NBUF == 2 ? (it & 1) : 0;
     const uint32_t use = NBUF == 2 ? (uint32_t)(it >> 1) : (uint32_t)it;
     if (!mbar_wait_warp(accf0 + 8u * buf, use & 1u, abort_flag, p.err)) break;
     tc_fence_after();
-    const int m = t.mt * 128 + q * 32 + lane;  // weight row within the group
+    const int m = t.mt * MT + row_off + q * 32 + lane;  // weight row within the group
     const bool mvalid = m < p.Mg;
     const uint32_t tb =
         tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * NPART * NACC * BN);
@@ -239,7 +251,7 @@ __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce0 + 8u * buf);
+      if (lane == 0) release(buf);
     } else {
       uint32_t pk[NCH][8];  // the unit's results, packed 16-bit pairs
 #pragma unroll
@@ -273,7 +285,7 @@ __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce0 + 8u * buf);  // TMEM free: stores follow
+      if (lane == 0) release(buf);  // TMEM free: stores follow
       if (mvalid) {
         uint16_t* out = static_cast<uint16_t*>(p.out);
 #pragma unroll
@@ -295,6 +307,22 @@ __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_
 }
 
 }  // namespace tc
+
+// Token-row maps of one operand for the SM-pair GEMMs: box[i] is (i + 1) * 16
+// rows high (up to 128, half of the largest tile), so each CTA brings its
+// share of a tile's token rows with one copy per K block.
+struct PairTokenMaps {
+  CUtensorMap box[8];
+};
+
+// The FFN's GEMMs on SM pairs (tc_gemm_pair.cu), weight maps with 128-row
+// boxes: gate/up with 160-row token tiles (token maps of x_perm), down with
+// bn = 160 or 256 (token maps of H).
+cudaError_t launch_gateup_pair(const CUtensorMap& tg, const CUtensorMap& tu,
+                               const PairTokenMaps& tx, const tc::Params& p, int P, int n_groups,
+                               cudaStream_t s);
+cudaError_t launch_down_pair(const CUtensorMap& td, const PairTokenMaps& th, const tc::Params& p,
+                             int bn, int P, int n_groups, cudaStream_t s);
 
 // Host: 2-D tiled tensor map (row-major [rows, inner] of `elsize`-byte elements),
 // boxes of box_rows x box_inner, with the given shared-memory swizzle (the MMA

@@ -243,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..9)
     tc::epilogue_loop<MODE, BN, C::NACC, C::NBUF>(p, total, m_tiles, KB, prefix, gstart,
-                                                  tmem_base, accf0, acce0, abort_flag, 2);
+                                                  tmem_base, accf0, acce0, abort_flag, 2,
+                                                  blockIdx.x, gridDim.x, 0);
   }
 
   tc_fence_before();
@@ -330,37 +331,54 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
                           cudaStream_t s, int n_mats, const int32_t* group_slot) {
   if (P == 0) return cudaSuccess;
   const uint64_t cap = (uint64_t)tc_row_capacity(P);
-  // Token tiles by mean batch size: 32 rows for decode-sized batches (deep
-  // pipelines); 160 rows while batches are up to a few hundred rows (a batch
-  // of 95-160 rows is one tile, so its weights pass once, with room for 4-6
-  // stages); 256 rows for larger batches (tensor bound: the largest MMA).
+  // Token tiles by mean batch size: 32 rows for decode-sized batches (one SM
+  // per tile, deep pipelines); 160 rows while batches are up to a few hundred
+  // rows (a batch of 95-160 rows is one tile, so its weights pass once); 256
+  // rows for larger batches (tensor bound: the largest MMA).  Large tiles run
+  // on SM pairs (tc_gemm_pair.cu), except gate/up with 256-row tiles: its two
+  // accumulators fill TMEM, and the pair's single buffer, released only when
+  // both CTAs' epilogues are done with it, stalls the MMA longer than on one
+  // SM, which measured faster there.
   const bool small = mean_rows <= 48.0;
   const int bn = small ? 32 : mean_rows <= 256.0 ? 160 : 256;
-  const int bn2 = bn;
-  // token operands: 32-row boxes for partial tiles, tile-high boxes for full ones
-  CUtensorMap tg, tu, tx, txf, td, th, thf, thf2;
   if (n_mats <= 0) n_mats = n_groups;
+  CUtensorMap tg, tu, td;
   if (!make_tmap(&tg, Wg, d, (uint64_t)n_mats * I, 128) ||
       !make_tmap(&tu, Wu, d, (uint64_t)n_mats * I, 128) ||
-      !make_tmap(&tx, x_perm, d, cap, 32) || !make_tmap(&txf, x_perm, d, cap, bn) ||
-      !make_tmap(&td, Wd, I, (uint64_t)n_mats * d, 128) || !make_tmap(&th, h, I, cap, 32) ||
-      !make_tmap(&thf, h, I, cap, 32) || !make_tmap(&thf2, h, I, cap, bn2))
+      !make_tmap(&td, Wd, I, (uint64_t)n_mats * d, 128))
     return cudaErrorInvalidValue;
   Params p1{offsets, n_groups, 0, I, d, h, I, nullptr, err, P, 0, 0, group_slot};
-  const long long u1 = (long long)((I + 127) / 128) * ((P + bn - 1) / bn + n_groups);
-  cudaError_t e;
-  if (small)
-    e = launch_tc<MODE_GATEUP, 32, 6>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
-  else if (bn == 160)
-    e = launch_tc<MODE_GATEUP, 160, 4>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
-  else
-    e = launch_tc<MODE_GATEUP, 256, 3>(tg, tu, tx, txf, p1, u1, "ffn_gateup_tc", s);
-  if (e != cudaSuccess) return e;
   Params p2{offsets, n_groups, 0, d, I, y_perm, d, slot_w, err, P, 0, 0, group_slot};
-  const long long u2 = (long long)((d + 127) / 128) * ((P + bn2 - 1) / bn2 + n_groups);
-  if (small) return launch_tc<MODE_DOWN, 32, 10>(td, td, th, thf, p2, u2, "ffn_down_tc", s);
-  if (bn2 == 160) return launch_tc<MODE_DOWN, 160, 6>(td, td, th, thf2, p2, u2, "ffn_down_tc", s);
-  return launch_tc<MODE_DOWN, 256, 4>(td, td, th, thf2, p2, u2, "ffn_down_tc", s);
+  const long long tiles = (long long)(P + bn - 1) / bn + n_groups;
+  if (small) {
+    // token operands: 32-row boxes (a tile is one box)
+    CUtensorMap tx, th;
+    if (!make_tmap(&tx, x_perm, d, cap, 32) || !make_tmap(&th, h, I, cap, 32))
+      return cudaErrorInvalidValue;
+    const cudaError_t e = launch_tc<MODE_GATEUP, 32, 6>(tg, tu, tx, tx, p1, (I + 127) / 128 * tiles,
+                                                        "ffn_gateup_tc", s);
+    if (e != cudaSuccess) return e;
+    return launch_tc<MODE_DOWN, 32, 10>(td, td, th, th, p2, (d + 127) / 128 * tiles, "ffn_down_tc",
+                                        s);
+  }
+  // SM pairs: one token box per CTA and K block, (i + 1) * 16 rows high
+  PairTokenMaps pxm, phm;
+  for (int i = 0; i < bn / 32; ++i)
+    if (!make_tmap(&pxm.box[i], x_perm, d, cap, 16 * (i + 1)) ||
+        !make_tmap(&phm.box[i], h, I, cap, 16 * (i + 1)))
+      return cudaErrorInvalidValue;
+  cudaError_t e;
+  if (bn == 160) {
+    e = launch_gateup_pair(tg, tu, pxm, p1, P, n_groups, s);
+  } else {  // one SM per tile: 32-row boxes for partial tiles, one 256-row box for full ones
+    CUtensorMap tx, txf;
+    if (!make_tmap(&tx, x_perm, d, cap, 32) || !make_tmap(&txf, x_perm, d, cap, 256))
+      return cudaErrorInvalidValue;
+    e = launch_tc<MODE_GATEUP, 256, 3>(tg, tu, tx, txf, p1, (I + 127) / 128 * tiles,
+                                       "ffn_gateup_tc", s);
+  }
+  if (e != cudaSuccess) return e;
+  return launch_down_pair(td, phm, p2, bn, P, n_groups, s);
 }
 
 cudaError_t launch_router_logits_tc(const void* x, const void* Wr, int T, int d, int E,

@@ -312,7 +312,8 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
     // ------------------------------------------------------------ epilogue (warps 3..10)
     tc::epilogue_loop<MODE, BN, C::NACC, C::NBUF, true, NI>(p, total, m_tiles, KB, prefix,
                                                             gstart, tmem_base, accf0, acce0,
-                                                            abort_flag, kFirstEpiWarp);
+                                                            abort_flag, kFirstEpiWarp,
+                                                            blockIdx.x, gridDim.x, 0);
   } else {
     // ------------------------------------------------------------ converters
     // Warp w may write only TMEM lanes 32 (w % 4) .. +31, so thread (w, lane)
