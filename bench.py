@@ -168,8 +168,8 @@ def kernel_bytes(cfg, kernel, n_active_all):
 def kernel_source_sha(kernel):
     """Hash of the CUDA sources a grouped-GEMM kernel is built from."""
     csrc = os.path.join(ROOT, "expert_dispatch_gb300", "csrc")
-    files = ["common.cuh", "tc_common.cuh",
-             "tc_gemm_q8.cu" if kernel.endswith("_q8") else "tc_gemm.cu"]
+    files = ["common.cuh", "tc_common.cuh"] + (
+        ["tc_gemm_q8.cu"] if kernel.endswith("_q8") else ["tc_gemm.cu", "tc_gemm_pair.cu"])
     h = hashlib.sha256()
     for name in files:
         with open(os.path.join(csrc, name), "rb") as f:

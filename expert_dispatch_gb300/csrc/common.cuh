@@ -253,9 +253,13 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
 }
+// Arrive on a barrier of either CTA of the cluster (a shared::cluster
+// address), with the default (CTA-scope release) semantics: what it hands over
+// is tensor-memory or shared-memory state whose order against the arrive is
+// set by the tcgen05 fences around it, and a cluster-scope release here would
+// drain the thread's memory operations at every arrive.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
 // TMA load into this CTA's shared memory whose completion is signalled on a
 // barrier of either CTA of the pair (a shared::cluster address).

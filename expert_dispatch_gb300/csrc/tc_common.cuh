@@ -83,6 +83,10 @@ __device__ __forceinline__ Unit decode_unit(int u, const int* prefix, const int*
   return r;
 }
 
+// SM pairs: MMA width of a unit with nt token rows, a multiple of 32 so each
+// CTA holds a multiple of 16 rows, brought by one box of that height.
+__device__ __forceinline__ int pair_n(int nt) { return max(32, (nt + 31) & ~31); }
+
 // One warp builds the schedule in shared memory.  Batch boundaries are made
 // safe first: each clamped to [0, max_rows] and forced non-decreasing
 // (running max), so every batch lies inside the row buffers whatever the
@@ -316,13 +320,13 @@ struct PairTokenMaps {
 };
 
 // The FFN's GEMMs on SM pairs (tc_gemm_pair.cu), weight maps with 128-row
-// boxes: gate/up with 160-row token tiles (token maps of x_perm), down with
-// bn = 160 or 256 (token maps of H).
+// boxes: gate/up with 160-row token tiles (token maps of x_perm, box[0..4]),
+// down with 256-row tiles (token maps of H, box[0..7]).
 cudaError_t launch_gateup_pair(const CUtensorMap& tg, const CUtensorMap& tu,
                                const PairTokenMaps& tx, const tc::Params& p, int P, int n_groups,
                                cudaStream_t s);
 cudaError_t launch_down_pair(const CUtensorMap& td, const PairTokenMaps& th, const tc::Params& p,
-                             int bn, int P, int n_groups, cudaStream_t s);
+                             int P, int n_groups, cudaStream_t s);
 
 // Host: 2-D tiled tensor map (row-major [rows, inner] of `elsize`-byte elements),
 // boxes of box_rows x box_inner, with the given shared-memory swizzle (the MMA

@@ -332,13 +332,15 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
   if (P == 0) return cudaSuccess;
   const uint64_t cap = (uint64_t)tc_row_capacity(P);
   // Token tiles by mean batch size: 32 rows for decode-sized batches (one SM
-  // per tile, deep pipelines); 160 rows while batches are up to a few hundred
-  // rows (a batch of 95-160 rows is one tile, so its weights pass once); 256
-  // rows for larger batches (tensor bound: the largest MMA).  Large tiles run
-  // on SM pairs (tc_gemm_pair.cu), except gate/up with 256-row tiles: its two
-  // accumulators fill TMEM, and the pair's single buffer, released only when
-  // both CTAs' epilogues are done with it, stalls the MMA longer than on one
-  // SM, which measured faster there.
+  // per tile, deep pipelines).  Larger batches: gate/up with 160-row tiles
+  // while batches are up to a few hundred rows (a batch of 95-160 rows is one
+  // tile, so its weights pass once), 256 beyond (tensor bound: the largest
+  // MMA); down always with 256-row tiles (fewer tiles per batch, so fewer
+  // passes over its weights: measured faster than 160 on prefill batches of
+  // ~140 rows).  Large tiles run on SM pairs (tc_gemm_pair.cu), except gate/up
+  // with 256-row tiles: its two accumulators fill TMEM, and the pair's single
+  // buffer, released only when both CTAs' epilogues are done with it, stalls
+  // the MMA longer than on one SM, which measured faster there.
   const bool small = mean_rows <= 48.0;
   const int bn = small ? 32 : mean_rows <= 256.0 ? 160 : 256;
   if (n_mats <= 0) n_mats = n_groups;
@@ -363,8 +365,8 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
   }
   // SM pairs: one token box per CTA and K block, (i + 1) * 16 rows high
   PairTokenMaps pxm, phm;
-  for (int i = 0; i < bn / 32; ++i)
-    if (!make_tmap(&pxm.box[i], x_perm, d, cap, 16 * (i + 1)) ||
+  for (int i = 0; i < 8; ++i)
+    if ((i < bn / 32 && !make_tmap(&pxm.box[i], x_perm, d, cap, 16 * (i + 1))) ||
         !make_tmap(&phm.box[i], h, I, cap, 16 * (i + 1)))
       return cudaErrorInvalidValue;
   cudaError_t e;
@@ -378,7 +380,7 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
                                        "ffn_gateup_tc", s);
   }
   if (e != cudaSuccess) return e;
-  return launch_down_pair(td, phm, p2, bn, P, n_groups, s);
+  return launch_down_pair(td, phm, p2, P, n_groups, s);
 }
 
 cudaError_t launch_router_logits_tc(const void* x, const void* Wr, int T, int d, int E,

@@ -39,6 +39,7 @@ namespace {
 using tc::MODE_DOWN;
 using tc::MODE_GATEUP;
 using tc::Params;
+using tc::pair_n;
 using tc::Unit;
 constexpr int kThreads = 32 * (2 + tc::kEpiWarps);  // producer, MMA, epilogue
 
@@ -65,10 +66,6 @@ struct CfgPair {
   static_assert(COLS <= 512, "TMEM columns");
   static_assert(SMEM_TOTAL <= 232448, "shared memory");
 };
-
-// MMA width of a unit with nt token rows: a multiple of 32, so each CTA holds
-// a multiple of 16 rows, brought by one box of that height.
-__device__ __forceinline__ int pair_n(int nt) { return max(32, (nt + 31) & ~31); }
 
 template <int MODE, int BN, int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -321,11 +318,9 @@ cudaError_t launch_gateup_pair(const CUtensorMap& tg, const CUtensorMap& tu,
 }
 
 cudaError_t launch_down_pair(const CUtensorMap& td, const PairTokenMaps& th, const tc::Params& p,
-                             int bn, int P, int n_groups, cudaStream_t s) {
-  const long long units = (long long)((p.Mg + 255) / 256) * ((P + bn - 1) / bn + n_groups);
-  if (bn == 160) return launch_pair<MODE_DOWN, 160, 7>(td, td, th, p, units, "ffn_down_tc", s);
-  if (bn == 256) return launch_pair<MODE_DOWN, 256, 6>(td, td, th, p, units, "ffn_down_tc", s);
-  return cudaErrorInvalidValue;
+                             int P, int n_groups, cudaStream_t s) {
+  const long long units = (long long)((p.Mg + 255) / 256) * ((P + 255) / 256 + n_groups);
+  return launch_pair<MODE_DOWN, 256, 6>(td, td, th, p, units, "ffn_down_tc", s);
 }
 
 }  // namespace moe
