@@ -170,10 +170,12 @@ __device__ __forceinline__ float dot16<float>(const uint4& a, const uint4& b) {
 
 // Router logits for small batches on CUDA cores.  One block per expert row
 // (blockIdx.x = e; blockIdx.y = K chunk when d is larger than one block keeps
-// in registers): the 8 warps split the chunk's 16-byte vectors, keep their
-// share of Wr[e] in registers, and dot it with every token's x; the 8 warp
-// sums are then added in warp order, so each logit slice is bit-reproducible.
-// Router weights are read exactly once.
+// in registers; blockIdx.z = a run of tok_per_block tokens, so that larger
+// batches still spread over the SMs): the 8 warps split the chunk's 16-byte
+// vectors, keep their share of Wr[e] in registers, and dot it with each of the
+// run's tokens; the 8 warp sums are then added in warp order, so each logit
+// slice is bit-reproducible whatever the split.  Router weights are read once
+// per token run.
 constexpr int kSplitMaxVecPerLane = 4;
 constexpr int kSplitTokChunk = 32;
 
@@ -181,6 +183,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) router_logits_splitk(const T* __restrict__ x,
                                                             const T* __restrict__ Wr, int ntok,
                                                             int d, int E, int kc,
+                                                            int tok_per_block,
                                                             float* __restrict__ partial) {
   pdl_wait();     // the predecessor grid is complete and visible
   pdl_trigger();  // dependents may launch (they wait for this grid in turn)
@@ -198,8 +201,9 @@ __global__ void __launch_bounds__(256) router_logits_splitk(const T* __restrict_
     const int v = warp * 32 + lane + 256 * i;
     w[i] = v < nvec ? __ldg(wrow + v) : make_uint4(0, 0, 0, 0);
   }
-  for (int tc = 0; tc < ntok; tc += kSplitTokChunk) {
-    const int nt = min(kSplitTokChunk, ntok - tc);
+  const int t_end = min(ntok, (int)(blockIdx.z + 1) * tok_per_block);
+  for (int tc = blockIdx.z * tok_per_block; tc < t_end; tc += kSplitTokChunk) {
+    const int nt = min(kSplitTokChunk, t_end - tc);
     for (int tl = 0; tl < nt; ++tl) {
       const uint4* xrow = reinterpret_cast<const uint4*>(x + (size_t)(tc + tl) * d + k0);
       float acc = 0.f;
@@ -353,16 +357,23 @@ cudaError_t launch_router_logits_splitk(int dtype, const void* x, const void* Wr
   const int vec = dtype == MOE_BF16 ? 8 : 4;
   if (kc % vec || kc > kSplitMaxVecPerLane * 256 * vec || (long long)kc * ksplit < d)
     return cudaErrorInvalidValue;
-  dim3 grid(E, ksplit), block(256);
+  // token runs (multiples of kSplitTokChunk) so that there are about two
+  // blocks per SM
+  const long long rows = (long long)E * ksplit;
+  const long long want = (2LL * num_sms() + rows - 1) / rows;
+  const int max_runs = (T + kSplitTokChunk - 1) / kSplitTokChunk;
+  const int runs = (int)(want < max_runs ? want : max_runs);
+  const int tok_per_block = ((T + runs - 1) / runs + kSplitTokChunk - 1) / kSplitTokChunk *
+                            kSplitTokChunk;
+  dim3 grid(E, ksplit, (T + tok_per_block - 1) / tok_per_block), block(256);
   ProfScope p("router_logits_splitk", s);
   if (dtype == MOE_BF16)
-    (void)launch_kernel(router_logits_splitk<__nv_bfloat16>, grid, block, 0, s, 
-        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(Wr), T, d, E, kc,
-        partial);
+    (void)launch_kernel(router_logits_splitk<__nv_bfloat16>, grid, block, 0, s,
+                        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(Wr),
+                        T, d, E, kc, tok_per_block, partial);
   else
     (void)launch_kernel(router_logits_splitk<float>, grid, block, 0, s, static_cast<const float*>(x),
-                                                       static_cast<const float*>(Wr), T, d, E,
-                                                       kc, partial);
+                        static_cast<const float*>(Wr), T, d, E, kc, tok_per_block, partial);
   return cudaGetLastError();
 }
 

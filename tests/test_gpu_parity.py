@@ -76,6 +76,8 @@ ROUTER_CASES = [
     LayerConfig("r_bf16_tc", T=300, d=192, E=130, I=64, k=8, zipf_s=1.2),
     LayerConfig("r_bf16_tc_sig", T=517, d=256, E=256, I=64, k=8, S=1, gate=1, norm_topk=1,
                 routed_scaling=2.827, sel_bias_range=0.1),
+    # CUDA-core router over several token runs per expert row (the last one ragged)
+    LayerConfig("r_bf16_simt_runs", T=600, d=320, E=40, I=64, k=4),
 ]
 
 
@@ -215,6 +217,42 @@ def test_expert_ffn_and_combine_parity(cfg):
     ref_y = oracle.combine(got, ref["slot_row"], cfg.k, cfg.S, w=w_ref.astype(np.float32),
                            residual=host(res))
     assert rel_err(host(y).numpy(), ref_y) <= 1e-6
+
+
+# Batch sizes chosen to land on every tile edge of the large-tile paths: 32-row
+# MMA widths (pair halves of 16 rows), 160-row tiles (SM-pair gate/up), 256-row
+# tiles (SM-pair down, one-SM gate/up), several tiles per batch, and weight
+# blocks of 256 rows that end inside a matrix (I = 320, d = 192).
+TILE_EDGE_CASES = [
+    ("pair160", LayerConfig("edges_pair160", T=689, d=256, E=10, I=320, k=2),
+     [1, 15, 16, 17, 33, 159, 160, 161, 300, 516]),
+    ("onesm256", LayerConfig("edges_onesm256", T=1216, d=192, E=8, I=320, k=2),
+     [1, 255, 256, 257, 600, 1000, 31, 32]),
+]
+
+
+@pytest.mark.parametrize("name,cfg,sizes", TILE_EDGE_CASES, ids=[c[0] for c in TILE_EDGE_CASES])
+def test_expert_ffn_tile_edges(name, cfg, sizes):
+    P = cfg.T * cfg.k
+    assert sum(sizes) == P and len(sizes) == cfg.E
+    inp = make_inputs(cfg, seed=11, device=DEV)
+    rng = np.random.default_rng(11)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    tok = rng.integers(0, cfg.T, size=P).astype(np.int32)
+    desc = moe.desc_from_config(cfg)
+    ws = moe.alloc_workspace(desc)
+    y_perm = torch.full((P, cfg.d), float("nan"), dtype=cfg.torch_dtype, device=DEV)
+    moe.moe_expert_ffn(desc, inp["x"], torch.from_numpy(off).to(DEV),
+                       torch.from_numpy(tok).to(DEV), None, inp["Wg"], inp["Wu"], inp["Wd"],
+                       y_perm, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    got = host(y_perm).double().numpy()
+    x_h = host(inp["x"])
+    for e in range(cfg.E):
+        ref = oracle.expert_rows(x_h, host(inp["Wg"][e]), host(inp["Wu"][e]), host(inp["Wd"][e]),
+                                 tok[off[e]:off[e + 1]])
+        err = rel_err(got[off[e]:off[e + 1]], ref)
+        assert err <= y_tol(cfg), (e, sizes[e], err)
 
 
 # ---------------------------------------------------------------- whole layer, small
