@@ -6,13 +6,16 @@
 // Same work units, MMA shape and epilogue as the bf16 kernel (tc_gemm.cu);
 // what changes is how a weight tile reaches the tensor core.  Per 64-wide K
 // block of a unit:
-//   * the weight loader (warp 0) brings the tile's int8 codes (128 rows x
-//     64 B, 64-byte swizzle) and f16 scales (2 blocks x 128 rows) into a
-//     weight stage (WS deep);
+//   * the weight loader (warp 0) brings the tile's int8 codes and f16 scales
+//     into a weight stage (WS deep), two K blocks per stage: 128 rows x 128 B
+//     of codes (128-byte swizzle) and 4 scale blocks x 128 rows, so each copy
+//     moves whole 128-byte code rows (with one 64-byte row per K block the
+//     down GEMM, one operand per stage, measured ~10 % slower);
 //   * the token loader (warp 2) brings the unit's token rows (fp16, 128-byte
 //     swizzle) into a token stage (TS deep);
 //   * converter warps read the codes and scales into registers and hand the
-//     weight stage straight back, then decode: scale * q rounded to fp16.
+//     weight stage straight back, then decode each of its K blocks in turn:
+//     scale * q rounded to fp16.
 //     The MMA takes its M-side operand from tensor memory (one weight row per
 //     TMEM lane, two 16-bit K elements per 32-bit column), so each converter
 //     thread owns one row of its warp's lane quarter and writes it with
@@ -29,9 +32,9 @@
 // so the in-flight depth of the weight stream does not shrink by the decode
 // and MMA latency; the weight loader never waits for the predecessor grid
 // (weights are never written by the kernel just before; the token rows are,
-// so the token loader waits).  The 64-byte swizzle puts 16-byte chunk j of
-// code row r at chunk j ^ ((r / 2) % 4), so the 32 rows a warp reads at once
-// fall in distinct banks.
+// so the token loader waits).  The 128-byte swizzle puts 16-byte chunk j of
+// code row r at chunk j ^ (r % 8), so a warp's 32 rows read one chunk each
+// in the minimum four shared-memory wavefronts.
 // The operands are fp16 because the decode then costs one byte permute, one
 // subtraction and one multiplication per two weights (packed half2); token
 // rows arrive in fp16 (converted from bf16 by the gather, exactly for values
@@ -61,8 +64,8 @@ constexpr int threads_q8(int NI) { return 32 * (kIssuer2 + NI - 1); }
 template <int MODE, int BN, int WS, int TS, int CS, int NI>
 struct CfgQ8 {
   static constexpr int NA = MODE == MODE_GATEUP ? 2 : 1;  // weight operands per K block
-  static constexpr int QA_BYTES = 128 * 64;               // int8 codes of one weight tile
-  static constexpr int SA_BYTES = 2 * 128 * 2;            // its f16 scales [2 blocks][128 rows]
+  static constexpr int QA_BYTES = 128 * 128;  // int8 codes of a weight tile: 128 rows x two K blocks
+  static constexpr int SA_BYTES = 4 * 128 * 2;  // its f16 scales [4 blocks][128 rows]
   static constexpr int SA_OFF = NA * QA_BYTES;            // scales inside a weight stage
   static constexpr int W_TX = NA * (QA_BYTES + SA_BYTES);  // bytes one weight stage receives
   static constexpr int W_BYTES = (W_TX + 1023) / 1024 * 1024;
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
         const int mat = tc::weight_mat(p, t.g);
         const int arow = mat * p.Mg + t.mt * 128;
         bool ok = true;
-        for (int kb = t.kb0; kb < t.kb1; ++kb) {
+        for (int kb = t.kb0; kb < t.kb1; kb += 2) {  // a stage holds K blocks kb, kb + 1
           if (!mbar_wait(w_empty(stage), phase ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
@@ -317,32 +320,35 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
   } else {
     // ------------------------------------------------------------ converters
     // Warp w may write only TMEM lanes 32 (w % 4) .. +31, so thread (w, lane)
-    // owns weight row r = 32 (w % 4) + lane and decodes its 64 weights of a
-    // K block.  Gate/up: the first four converter warps decode operand 0,
-    // the other four operand 1.  Down: the first four take the even K blocks
-    // of this CTA's sequence, the other four the odd ones, so two K blocks
-    // are in conversion at once (a down K block is half the bytes of a
-    // gate/up one, and one at a time left the converters short of the
-    // weight stream).
-    constexpr int NCH = 4;  // 16-byte code chunks per thread: a 64-weight row
+    // owns weight row r = 32 (w % 4) + lane: per weight stage it reads its
+    // row's 128 codes (two K blocks) and four scales, hands the stage back,
+    // then decodes and writes one converted K block at a time.  Gate/up: the
+    // first four converter warps decode operand 0, the other four operand 1.
+    // Down: the first four take the even weight stages of this CTA's
+    // sequence, the other four the odd ones, so two stages are in conversion
+    // at once (a down stage is half the bytes of a gate/up one, and one at a
+    // time left the converters short of the weight stream).
+    constexpr int NCH = 8;  // 16-byte code chunks per thread: a 128-weight row
     const int cw = warp - kFirstConvWarp;
     const int q = warp & 3, r = q * 32 + lane;
     const int op = C::NA == 2 ? cw >> 2 : 0;
-    const uint32_t group = C::NA == 2 ? 0u : (uint32_t)(cw >> 2);  // down: K-block parity
-    const int j0 = 0;
-    const int swz = (r >> 1) & 3;
-    const int code_off = op * C::QA_BYTES + r * 64;
+    const uint32_t group = C::NA == 2 ? 0u : (uint32_t)(cw >> 2);  // down: stage parity
+    const int swz = r & 7;  // 128-byte swizzle: chunk j of code row r sits at j ^ (r % 8)
+    const int code_off = op * C::QA_BYTES + r * 128;
     const int scale_off = C::SA_OFF + op * C::SA_BYTES + r * 2;  // + scale block * 256
-    const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) +
-                           (uint32_t)(C::ACC_COLS + op * 32 + j0 * 8);
-    uint32_t kcount = 0;
+    const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::ACC_COLS + op * 32);
+    uint32_t kcount = 0, wcount = 0;  // K blocks and weight stages seen so far
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit t = tc::decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
-      for (int kb = t.kb0; kb < t.kb1; ++kb, ++kcount) {
-        if (C::NA == 1 && (kcount & 1u) != group) continue;
-        const int ws = kcount % WS, cs = kcount % CS;
-        if (!tc::mbar_wait_warp(w_full(ws), (kcount / WS) & 1u, abort_flag, p.err)) {
+      for (int kb = t.kb0; kb < t.kb1 && ok; kb += 2, ++wcount) {
+        const int nk = min(2, t.kb1 - kb);  // K blocks in this stage
+        if (C::NA == 1 && (wcount & 1u) != group) {
+          kcount += nk;
+          continue;
+        }
+        const int ws = wcount % WS;
+        if (!tc::mbar_wait_warp(w_full(ws), (wcount / WS) & 1u, abort_flag, p.err)) {
           ok = false;
           break;
         }
@@ -351,37 +357,45 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
         __half sh[NCH / 2];
 #pragma unroll
         for (int i = 0; i < NCH; ++i)
-          codes[i] = *reinterpret_cast<const uint4*>(w + code_off + (((j0 + i) ^ swz) << 4));
+          codes[i] = *reinterpret_cast<const uint4*>(w + code_off + ((i ^ swz) << 4));
 #pragma unroll
         for (int b = 0; b < NCH / 2; ++b)
-          sh[b] = *reinterpret_cast<const __half*>(w + scale_off + ((j0 >> 1) + b) * 256);
+          sh[b] = *reinterpret_cast<const __half*>(w + scale_off + b * 256);
         __syncwarp();  // the warp's reads of the stage are done: hand it back
         if (lane == 0) mbar_arrive(w_empty(ws));
-        if (!tc::mbar_wait_warp(conv_empty(cs), ((kcount / CS) & 1u) ^ 1u, abort_flag, p.err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t o[NCH * 8];
 #pragma unroll
-        for (int i = 0; i < NCH; ++i) {
-          const __half2 s2 = __halves2half2(sh[i >> 1], sh[i >> 1]);
-          const uint4 lo = dequant8_f16(make_uint2(codes[i].x, codes[i].y), s2);
-          const uint4 hi = dequant8_f16(make_uint2(codes[i].z, codes[i].w), s2);
-          o[8 * i + 0] = lo.x;
-          o[8 * i + 1] = lo.y;
-          o[8 * i + 2] = lo.z;
-          o[8 * i + 3] = lo.w;
-          o[8 * i + 4] = hi.x;
-          o[8 * i + 5] = hi.y;
-          o[8 * i + 6] = hi.z;
-          o[8 * i + 7] = hi.w;
+        for (int h = 0; h < 2; ++h) {
+          if (h >= nk) break;
+          const int cs = kcount % CS;
+          if (!tc::mbar_wait_warp(conv_empty(cs), ((kcount / CS) & 1u) ^ 1u, abort_flag,
+                                  p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t o[32];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = 4 * h + i;  // code chunk: 16 codes, scale block c / 2
+            const __half2 s2 = __halves2half2(sh[c >> 1], sh[c >> 1]);
+            const uint4 lo = dequant8_f16(make_uint2(codes[c].x, codes[c].y), s2);
+            const uint4 hi = dequant8_f16(make_uint2(codes[c].z, codes[c].w), s2);
+            o[8 * i + 0] = lo.x;
+            o[8 * i + 1] = lo.y;
+            o[8 * i + 2] = lo.z;
+            o[8 * i + 3] = lo.w;
+            o[8 * i + 4] = hi.x;
+            o[8 * i + 5] = hi.y;
+            o[8 * i + 6] = hi.z;
+            o[8 * i + 7] = hi.w;
+          }
+          tmem_st32(t_row + (uint32_t)(cs * C::NA * 32), o);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(conv_full(cs));
+          ++kcount;
         }
-        tmem_st32(t_row + (uint32_t)(cs * C::NA * 32), o);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(conv_full(cs));
       }
     }
   }
@@ -401,14 +415,14 @@ bool make_f16_map(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t ro
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// codes [n_groups * R, K] int8 in 128 x 64 boxes, 64-byte swizzle; scales
-// [n_groups * K/32, R] f16 in 2 x 128 boxes
+// codes [n_groups * R, K] int8 in 128 x 128 boxes (two K blocks), 128-byte
+// swizzle; scales [n_groups * K/32, R] f16 in 4 x 128 boxes
 bool make_q8_maps(CUtensorMap* tq, CUtensorMap* ts, const Q8Weight& w, int n_groups, int R,
                   int K) {
-  return make_tmap_2d(tq, w.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, (uint64_t)n_groups * R, 64,
-                      128, CU_TENSOR_MAP_SWIZZLE_64B) &&
+  return make_tmap_2d(tq, w.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, (uint64_t)n_groups * R, 128,
+                      128, CU_TENSOR_MAP_SWIZZLE_128B) &&
          make_tmap_2d(ts, w.scale, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, R,
-                      (uint64_t)n_groups * (K / 32), 128, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+                      (uint64_t)n_groups * (K / 32), 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <int MODE, int BN, int WS, int TS, int CS, int NI>
@@ -458,14 +472,14 @@ cudaError_t launch_ffn_tc_q8(const void* x_perm, const int32_t* offsets, int n_g
   const long long u1 = (long long)((I + 127) / 128) * ((P + bn - 1) / bn + n_groups);
   const char* n1 = "ffn_gateup_tc_q8";
   const cudaError_t e =
-      small ? launch_q8<MODE_GATEUP, 32, 10, 8, 4, 2>(qg, qu, sg, su, tx, txf, p1, u1, n1, s)
-            : launch_q8<MODE_GATEUP, 128, 8, 4, 4, 1>(qg, qu, sg, su, tx, txf, p1, u1, n1, s);
+      small ? launch_q8<MODE_GATEUP, 32, 5, 8, 4, 2>(qg, qu, sg, su, tx, txf, p1, u1, n1, s)
+            : launch_q8<MODE_GATEUP, 128, 4, 4, 4, 1>(qg, qu, sg, su, tx, txf, p1, u1, n1, s);
   if (e != cudaSuccess) return e;
   Params p2{offsets, n_groups, 0, d, I, y_perm, d, slot_w, err, P};
   const long long u2 = (long long)((d + 127) / 128) * ((P + bn2 - 1) / bn2 + n_groups);
   const char* n2 = "ffn_down_tc_q8";
-  return small ? launch_q8<MODE_DOWN, 32, 18, 8, 8, 4>(qd, qd, sd, sd, th, th, p2, u2, n2, s)
-               : launch_q8<MODE_DOWN, 256, 12, 3, 8, 1>(qd, qd, sd, sd, th, thf2, p2, u2, n2, s);
+  return small ? launch_q8<MODE_DOWN, 32, 10, 8, 8, 4>(qd, qd, sd, sd, th, th, p2, u2, n2, s)
+               : launch_q8<MODE_DOWN, 256, 6, 3, 8, 1>(qd, qd, sd, sd, th, thf2, p2, u2, n2, s);
 }
 
 }  // namespace moe
