@@ -114,6 +114,21 @@ cudaEvent_t take_event() {
 }
 
 // The routing passes and the shared gating kernel.
+// Routing and the dispatch plan of a layer call (no slot weights: the combine
+// applies the gate weights).
+moe_status do_route(const moe_layer_desc* D, const void* x, const void* Wr,
+                    const float* logit_bias, const float* sel_bias, int32_t* ids, float* w,
+                    const Ws& W, cudaStream_t s);
+moe_status route_and_plan(const moe_layer_desc* D, const void* x, const void* Wr,
+                          const float* logit_bias, const float* sel_bias, int32_t* ids, float* w,
+                          const Ws& W, cudaStream_t s) {
+  const moe_status st = do_route(D, x, Wr, logit_bias, sel_bias, ids, w, W, s);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_plan(ids, nullptr, D->T, D->E, D->k, D->S, W.offsets, W.tok_idx,
+                                 W.slot_row, W.active, W.n_active, nullptr, W.bits, W.wpre,
+                                 W.counts, W.flags, s));
+}
+
 moe_status do_route(const moe_layer_desc* D, const void* x, const void* Wr,
                     const float* logit_bias, const float* sel_bias, int32_t* ids, float* w,
                     const Ws& W, cudaStream_t s) {
@@ -506,11 +521,7 @@ moe_status moe_layer_forward_q8(const moe_layer_desc* desc, const void* x, const
   int32_t* ids = topk_ids_out ? topk_ids_out : W.topk_ids;
   float* w = topk_w_out ? topk_w_out : W.topk_w;
   if (cudaMemsetAsync(W.flags, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((st = do_route(desc, x, Wr, logit_bias, sel_bias, ids, w, W, s)) != MOE_OK) return st;
-  if (launch_plan(ids, nullptr, desc->T, desc->E, desc->k, desc->S, W.offsets, W.tok_idx,
-                  W.slot_row, W.active, W.n_active, nullptr, W.bits, W.wpre, W.counts, W.flags,
-                  s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if ((st = route_and_plan(desc, x, Wr, logit_bias, sel_bias, ids, w, W, s)) != MOE_OK) return st;
   if ((st = do_ffn_q8(desc, x, W.offsets, W.tok_idx, W.slot_row, nullptr, Wg, Wu, Wd, W.y_perm,
                       W, s)) !=
       MOE_OK)
@@ -557,11 +568,7 @@ moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const vo
   int32_t* ids = topk_ids_out ? topk_ids_out : W.topk_ids;
   float* w = topk_w_out ? topk_w_out : W.topk_w;
   if (cudaMemsetAsync(W.flags, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((st = do_route(desc, x, Wr, logit_bias, sel_bias, ids, w, W, s)) != MOE_OK) return st;
-  if (launch_plan(ids, nullptr, desc->T, desc->E, desc->k, desc->S, W.offsets, W.tok_idx,
-                  W.slot_row, W.active, W.n_active, nullptr, W.bits, W.wpre, W.counts, W.flags,
-                  s) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if ((st = route_and_plan(desc, x, Wr, logit_bias, sel_bias, ids, w, W, s)) != MOE_OK) return st;
   if ((st = do_ffn(desc, x, W.offsets, W.tok_idx, W.slot_row, nullptr, Wg, Wu, Wd, W.y_perm, W,
                    s)) != MOE_OK)
     return st;
@@ -696,11 +703,8 @@ moe_status moe_tier_forward(moe_expert_tier* tier, const moe_layer_desc* desc, c
   if (tier->done_recorded && cudaStreamWaitEvent(s, tier->done, 0) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (cudaMemsetAsync(W.flags, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((st = do_route(desc, x, Wr, logit_bias, sel_bias, ids, w, W, s)) != MOE_OK) return st;
-  if (launch_plan(ids, nullptr, desc->T, desc->E, desc->k, desc->S, W.offsets, W.tok_idx,
-                  W.slot_row, W.active, W.n_active, nullptr, W.bits, W.wpre, W.counts, W.flags,
-                  s) != cudaSuccess ||
-      permute_rows(desc, false, x, W.offsets, W.tok_idx, W.slot_row, W, s) != cudaSuccess)
+  if ((st = route_and_plan(desc, x, Wr, logit_bias, sel_bias, ids, w, W, s)) != MOE_OK) return st;
+  if (permute_rows(desc, false, x, W.offsets, W.tok_idx, W.slot_row, W, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   // the routing decision reaches the host: batch bounds per expert
   int32_t* bounds = tier->host_tab;

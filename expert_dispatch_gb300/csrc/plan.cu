@@ -16,13 +16,10 @@
 // Every result is a pure function of the routing (bit-reproducible).
 #include "common.cuh"
 #include "internal.h"
+#include "route_plan.cuh"
 
 namespace moe {
 namespace {
-
-__device__ __forceinline__ int pair_expert(const int32_t* ids, int t, int j, int k, int E) {
-  return j < k ? ids[(size_t)t * k + j] : E + (j - k);
-}
 
 __global__ void plan_mark(const int32_t* __restrict__ ids, int T, int E, int k, int S,
                           uint32_t* __restrict__ bits, int nw, int* __restrict__ flags) {
@@ -32,7 +29,7 @@ __global__ void plan_mark(const int32_t* __restrict__ ids, int T, int E, int k, 
   const int ks = k + S;
   if (p >= (long long)T * ks) return;
   const int t = (int)(p / ks), j = (int)(p % ks);
-  const int e = pair_expert(ids, t, j, k, E);
+  const int e = rp::pair_expert(ids, t, j, k, E);
   if (j < k && (e < 0 || e >= E)) {
     flag_error(flags, kErrDeviceInput);
     return;
@@ -138,7 +135,7 @@ __global__ void plan_place(const int32_t* __restrict__ ids, const float* __restr
   const int ks = k + S;
   if (p >= (long long)T * ks) return;
   const int t = (int)(p / ks), j = (int)(p % ks);
-  const int e = pair_expert(ids, t, j, k, E);
+  const int e = rp::pair_expert(ids, t, j, k, E);
   if (j < k && (e < 0 || e >= E)) {
     slot_row[p] = -1;
     return;
@@ -151,38 +148,9 @@ __global__ void plan_place(const int32_t* __restrict__ ids, const float* __restr
   if (slot_w) slot_w[pos] = (j < k && topk_w) ? topk_w[(size_t)t * k + j] : 1.f;
 }
 
-// Block-wide exclusive scan for any blockDim.x that is a multiple of 32.
-__device__ int block_exclusive_scan_any(int v, int* warp_sums, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int s = lane < nwarps ? warp_sums[lane] : 0;
-    int si = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int u = __shfl_up_sync(0xffffffffu, si, o);
-      if (lane >= o) si += u;
-    }
-    if (lane < nwarps) warp_sums[lane] = si - s;
-    if (lane == 31) *total = si;
-  }
-  __syncthreads();
-  const int r = warp_sums[warp] + incl - v;
-  __syncthreads();
-  return r;
-}
-
-// The whole plan in one block, for problems whose token bitmaps fit in
-// shared memory: the three steps above with the bitmaps, word prefixes and
-// offsets kept on chip.  Same results, one launch.
+// The whole plan in one block (rp::plan_block), for problems whose token
+// bitmaps fit in shared memory: the three steps above with the bitmaps, word
+// prefixes and offsets kept on chip.  Same results, one launch.
 constexpr int kSmallPlanThreads = 1024;
 constexpr int kSmallPlanMaxWords = 4096;
 
@@ -196,72 +164,9 @@ __global__ void __launch_bounds__(kSmallPlanThreads) plan_small(
   extern __shared__ uint32_t sm[];
   __shared__ int warp_sums[32];
   __shared__ int chunk_total;
-  const int nE = E + S, ks = k + S;
-  const int nwords = nE * nw;
-  uint32_t* bits = sm;
-  int* wpre = reinterpret_cast<int*>(sm + nwords);
-  int* off = wpre + nwords;  // nE + 1
-  const int P = T * ks;
-  for (int i = threadIdx.x; i < nwords; i += blockDim.x) bits[i] = 0;
-  __syncthreads();
-  for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    const int t = p / ks, j = p - t * ks;
-    const int e = pair_expert(ids, t, j, k, E);
-    if (j < k && (e < 0 || e >= E)) {
-      flag_error(flags, kErrDeviceInput);
-      continue;
-    }
-    const uint32_t bit = 1u << (t & 31);
-    if (atomicOr(&bits[e * nw + (t >> 5)], bit) & bit) flag_error(flags, kErrDeviceInput);
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < nE; e += blockDim.x) {
-    int run = 0;
-    for (int w = 0; w < nw; ++w) {
-      wpre[e * nw + w] = run;
-      run += __popc(bits[e * nw + w]);
-    }
-    off[e] = run;  // batch size for now
-  }
-  __syncthreads();
-  int base = 0, abase = 0;
-  for (int e0 = 0; e0 < nE; e0 += blockDim.x) {
-    const int e = e0 + threadIdx.x;
-    const int c = e < nE ? off[e] : 0;
-    const int ex = block_exclusive_scan_any(c, warp_sums, &chunk_total);
-    if (e < nE) {
-      off[e] = base + ex;
-      offsets[e] = base + ex;
-    }
-    base += chunk_total;
-    __syncthreads();
-    const int a = (e < nE && c > 0) ? 1 : 0;
-    const int aex = block_exclusive_scan_any(a, warp_sums, &chunk_total);
-    if (a && active) active[abase + aex] = e;
-    abase += chunk_total;
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    off[nE] = base;
-    offsets[nE] = base;
-    if (n_active) *n_active = abase;
-  }
-  __syncthreads();
-  for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    const int t = p / ks, j = p - t * ks;
-    const int e = pair_expert(ids, t, j, k, E);
-    if (j < k && (e < 0 || e >= E)) {
-      slot_row[p] = -1;
-      continue;
-    }
-    const int wi = e * nw + (t >> 5);
-    const int pos = off[e] + wpre[wi] + __popc(bits[wi] & ((1u << (t & 31)) - 1u));
-    tok_idx[pos] = t;
-    slot_row[p] = pos;
-    if (slot_w) slot_w[pos] = (j < k && topk_w) ? topk_w[(size_t)t * k + j] : 1.f;
-  }
+  rp::plan_block(ids, topk_w, T, E, k, S, nw, offsets, tok_idx, slot_row, active, n_active, slot_w,
+                 flags, sm, warp_sums, &chunk_total);
 }
-
 }  // namespace
 
 cudaError_t launch_plan(const int32_t* ids, const float* topk_w, int T, int E, int k, int S,

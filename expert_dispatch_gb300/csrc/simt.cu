@@ -12,6 +12,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "route_plan.cuh"
 
 namespace moe {
 namespace {
@@ -145,40 +146,8 @@ __global__ void __launch_bounds__(256) simt_grouped_gemm_nt(
 // the router weights are read exactly once; partial[chunk][t][e] is summed in
 // chunk order by the top-k kernel (deterministic).  kc is a multiple of 32
 // 16-byte vectors' worth of elements (kc <= 4 * 32 * vector width).
-template <typename T>
-__device__ __forceinline__ float dot16(const uint4& a, const uint4& b);
-template <>
-__device__ __forceinline__ float dot16<__nv_bfloat16>(const uint4& a, const uint4& b) {
-  const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-  const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 fa = __bfloat1622float2(pa[i]), fb = __bfloat1622float2(pb[i]);
-    s = fmaf(fa.x, fb.x, s);
-    s = fmaf(fa.y, fb.y, s);
-  }
-  return s;
-}
-template <>
-__device__ __forceinline__ float dot16<float>(const uint4& a, const uint4& b) {
-  float s = __uint_as_float(a.x) * __uint_as_float(b.x);
-  s = fmaf(__uint_as_float(a.y), __uint_as_float(b.y), s);
-  s = fmaf(__uint_as_float(a.z), __uint_as_float(b.z), s);
-  return fmaf(__uint_as_float(a.w), __uint_as_float(b.w), s);
-}
-
-// Router logits for small batches on CUDA cores.  One block per expert row
-// (blockIdx.x = e; blockIdx.y = K chunk when d is larger than one block keeps
-// in registers; blockIdx.z = a run of tok_per_block tokens, so that larger
-// batches still spread over the SMs): the 8 warps split the chunk's 16-byte
-// vectors, keep their share of Wr[e] in registers, and dot it with each of the
-// run's tokens; the 8 warp sums are then added in warp order, so each logit
-// slice is bit-reproducible whatever the split.  Router weights are read once
-// per token run.
-constexpr int kSplitMaxVecPerLane = 4;
-constexpr int kSplitTokChunk = 32;
-
+// Router logits for small batches on CUDA cores (rp::router_logits_block):
+// grid (E, K chunks, token runs), 256 threads.
 template <typename T>
 __global__ void __launch_bounds__(256) router_logits_splitk(const T* __restrict__ x,
                                                             const T* __restrict__ Wr, int ntok,
@@ -187,57 +156,11 @@ __global__ void __launch_bounds__(256) router_logits_splitk(const T* __restrict_
                                                             float* __restrict__ partial) {
   pdl_wait();     // the predecessor grid is complete and visible
   pdl_trigger();  // dependents may launch (they wait for this grid in turn)
-  constexpr int VEC = 16 / sizeof(T);
-  __shared__ float wsum[8][kSplitTokChunk];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x;
-  const int chunk = blockIdx.y;
-  const int k0 = chunk * kc;
-  const int nvec = (min(d, k0 + kc) - k0) / VEC;
-  const uint4* wrow = reinterpret_cast<const uint4*>(Wr + (size_t)e * d + k0);
-  uint4 w[kSplitMaxVecPerLane];
-#pragma unroll
-  for (int i = 0; i < kSplitMaxVecPerLane; ++i) {
-    const int v = warp * 32 + lane + 256 * i;
-    w[i] = v < nvec ? __ldg(wrow + v) : make_uint4(0, 0, 0, 0);
-  }
-  const int t_end = min(ntok, (int)(blockIdx.z + 1) * tok_per_block);
-  for (int tc = blockIdx.z * tok_per_block; tc < t_end; tc += kSplitTokChunk) {
-    const int nt = min(kSplitTokChunk, t_end - tc);
-    for (int tl = 0; tl < nt; ++tl) {
-      const uint4* xrow = reinterpret_cast<const uint4*>(x + (size_t)(tc + tl) * d + k0);
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < kSplitMaxVecPerLane; ++i) {
-        const int v = warp * 32 + lane + 256 * i;
-        if (v < nvec) acc += dot16<T>(w[i], __ldg(xrow + v));
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) wsum[warp][tl] = acc;
-    }
-    __syncthreads();
-    if (threadIdx.x < nt) {
-      float s = 0.f;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) s += wsum[q][threadIdx.x];
-      partial[((size_t)chunk * ntok + tc + threadIdx.x) * E + e] = s;
-    }
-    __syncthreads();
-  }
+  rp::router_logits_block<T>(x, Wr, ntok, d, E, kc, tok_per_block, blockIdx.x, blockIdx.y,
+                             blockIdx.z, partial);
 }
 
-// tpb (1 or 8) tokens per block.  First the whole block forms the logits in shared
-// memory: logit = (sum over K chunks of the partial logits, in chunk order)
-// + the optional per-expert logit bias.  Then one warp per token: selection
-// score = logit (softmax family) or sigmoid(logit) + sel_bias (sigmoid
-// family); k rounds of a warp arg-max pick the experts in descending score
-// (ties and NaNs resolved toward the lower index).  Each lane caches the best
-// of its own PL experts, so a round is one warp arg-max plus a rescan by the
-// lane that lost its best.
-constexpr int kTopkTokens = 8;
-constexpr int kTopkMaxExperts = 1024;
-
+// tpb (1 or 8) tokens per block (rp::topk_tokens).
 template <int PL>  // experts per lane: E <= 32 * PL
 __global__ void __launch_bounds__(256) router_topk_kernel(
     const float* __restrict__ partial, int ksplit, const float* __restrict__ logit_bias,
@@ -245,126 +168,34 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     float rs, int32_t* __restrict__ ids, float* __restrict__ w) {
   pdl_wait();     // the predecessor grid is complete and visible
   pdl_trigger();  // dependents may launch (they wait for this grid in turn)
-  __shared__ float lg_s[kTopkTokens][32 * PL];
-  const int lane = threadIdx.x & 31;
+  __shared__ float lg_s[rp::kTopkTokens][32 * PL];
+  __shared__ float sb_s[32 * PL];
   const int t0 = blockIdx.x * tpb;
-  const int ntok = min(tpb, T - t0);
-  for (int idx = threadIdx.x; idx < ntok * E; idx += blockDim.x) {
-    const int tl = idx / E, e = idx - tl * E;
-    const float* src = partial + (size_t)(t0 + tl) * E + e;
-    float l = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < ksplit; ++c) l += src[(size_t)c * T * E];
-    lg_s[tl][e] = l + (logit_bias ? logit_bias[e] : 0.f);
-  }
-  __syncthreads();
-  const int tl = threadIdx.x >> 5;
-  const int t = t0 + tl;
-  if (tl >= ntok) return;
-  float lg[PL], sc[PL];
-  uint32_t taken = 0;
-#pragma unroll
-  for (int i = 0; i < PL; ++i) {
-    const int e = lane + 32 * i;
-    float l = -INFINITY, s = -INFINITY;
-    if (e < E) {
-      l = lg_s[tl][e];
-      s = gate == MOE_GATE_SOFTMAX_TOPK ? l
-                                        : 1.f / (1.f + expf(-l)) + (sel_bias ? sel_bias[e] : 0.f);
-      if (s != s) s = -INFINITY;
-    } else {
-      taken |= 1u << i;  // not an expert
-    }
-    lg[i] = l;
-    sc[i] = s;
-  }
-  // softmax normaliser over all experts
-  float m = -INFINITY, z = 0.f;
-  if (gate == MOE_GATE_SOFTMAX_TOPK) {
-#pragma unroll
-    for (int i = 0; i < PL; ++i) m = fmaxf(m, lg[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-#pragma unroll
-    for (int i = 0; i < PL; ++i)
-      if (lane + 32 * i < E) z += expf(lg[i] - m);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  }
-  // best untaken expert of this lane
-  float lbv = -INFINITY, lbl = 0.f;
-  int lbe = 0x7fffffff;
-  auto rescan = [&]() {
-    lbv = -INFINITY;
-    lbe = 0x7fffffff;
-    lbl = 0.f;
-#pragma unroll
-    for (int i = 0; i < PL; ++i) {
-      const int e = lane + 32 * i;
-      if (!((taken >> i) & 1u) && (sc[i] > lbv || (sc[i] == lbv && e < lbe))) {
-        lbv = sc[i];
-        lbe = e;
-        lbl = lg[i];
-      }
-    }
-  };
-  rescan();
-  int my_id = 0;
-  float my_w = 0.f;
-  for (int j = 0; j < k; ++j) {
-    float bv = lbv, bl = lbl;
-    int be = lbe;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      const float ol = __shfl_xor_sync(0xffffffffu, bl, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-        bl = ol;
-      }
-    }
-    if ((be & 31) == lane) {  // the owning lane retires it and finds its next best
-      taken |= 1u << (be >> 5);
-      rescan();
-    }
-    const float wj = gate == MOE_GATE_SOFTMAX_TOPK ? expf(bl - m) / z : 1.f / (1.f + expf(-bl));
-    if (lane == j) {
-      my_id = be;
-      my_w = wj;
-    }
-  }
-  if (norm_topk) {
-    const float s = lane < k ? my_w : 0.f;
-    // fixed-order sum over the selected slots (slot 0 first)
-    float tot = 0.f;
-    for (int j = 0; j < k; ++j) tot += __shfl_sync(0xffffffffu, s, j);
-    my_w = my_w / tot;
-  }
-  if (lane < k) {
-    ids[(size_t)t * k + lane] = my_id;
-    w[(size_t)t * k + lane] = rs * my_w;
-  }
+  rp::topk_tokens<PL>(partial, ksplit, logit_bias, sel_bias, T, t0, min(tpb, T - t0), E, k, gate,
+                      norm_topk, rs, ids, w, lg_s, sb_s);
 }
 
 }  // namespace
+
+// Tokens per block of the CUDA-core router grid: runs of whole
+// rp::kSplitTokChunk chunks, as many as give about two blocks per SM.
+int splitk_tokens_per_block(int T, int E, int ksplit) {
+  const long long rows = (long long)E * ksplit;
+  const long long want = (2LL * num_sms() + rows - 1) / rows;
+  const int max_runs = (T + rp::kSplitTokChunk - 1) / rp::kSplitTokChunk;
+  const int runs = (int)(want < max_runs ? want : max_runs);
+  return ((T + runs - 1) / runs + rp::kSplitTokChunk - 1) / rp::kSplitTokChunk *
+         rp::kSplitTokChunk;
+}
 
 cudaError_t launch_router_logits_splitk(int dtype, const void* x, const void* Wr, int T, int d,
                                         int E, int kc, int ksplit, float* partial,
                                         cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const int vec = dtype == MOE_BF16 ? 8 : 4;
-  if (kc % vec || kc > kSplitMaxVecPerLane * 256 * vec || (long long)kc * ksplit < d)
+  if (kc % vec || kc > rp::kSplitMaxVecPerLane * 256 * vec || (long long)kc * ksplit < d)
     return cudaErrorInvalidValue;
-  // token runs (multiples of kSplitTokChunk) so that there are about two
-  // blocks per SM
-  const long long rows = (long long)E * ksplit;
-  const long long want = (2LL * num_sms() + rows - 1) / rows;
-  const int max_runs = (T + kSplitTokChunk - 1) / kSplitTokChunk;
-  const int runs = (int)(want < max_runs ? want : max_runs);
-  const int tok_per_block = ((T + runs - 1) / runs + kSplitTokChunk - 1) / kSplitTokChunk *
-                            kSplitTokChunk;
+  const int tok_per_block = splitk_tokens_per_block(T, E, ksplit);
   dim3 grid(E, ksplit, (T + tok_per_block - 1) / tok_per_block), block(256);
   ProfScope p("router_logits_splitk", s);
   if (dtype == MOE_BF16)
@@ -383,7 +214,7 @@ cudaError_t launch_router_topk(const float* partial, int ksplit, const float* lo
   if (T == 0) return cudaSuccess;
   ProfScope p("router_topk", s);
   // small batches: one token per block so that the partial sums spread over many SMs
-  const int tpb = T < 8 * 152 ? 1 : kTopkTokens;
+  const int tpb = T < 8 * 152 ? 1 : rp::kTopkTokens;
   const int nb = (T + tpb - 1) / tpb;
 #define MOE_TOPK(PL)                                                                   \
   (void)launch_kernel(router_topk_kernel<PL>, nb, 256, 0, s, partial, ksplit, logit_bias, sel_bias, T, \

@@ -255,6 +255,39 @@ def test_expert_ffn_tile_edges(name, cfg, sizes):
         assert err <= y_tol(cfg), (e, sizes[e], err)
 
 
+# The routing inside a layer call equals the separate router call bit for bit
+# (ids and gate weights), and a second layer call on the same workspace
+# repeats the first exactly.
+ROUTE_REPEAT_CASES = [
+    LayerConfig("fr_one_token", T=1, d=512, E=32, I=64, k=4, S=1, gate=1, norm_topk=1,
+                routed_scaling=2.8, sel_bias_range=0.1),
+    LayerConfig("fr_fp32_ragged", T=37, d=72, E=5, I=36, k=3, S=1, dtype="f32", gate=1,
+                norm_topk=1, routed_scaling=2.0, sel_bias_range=0.1),
+    LayerConfig("fr_max_experts", T=40, d=128, E=1024, I=64, k=32, S=4, norm_topk=1),
+]
+
+
+@pytest.mark.parametrize("cfg", ROUTE_REPEAT_CASES, ids=lambda c: c.name)
+def test_layer_routing_matches_router_call_and_repeats(cfg):
+    inp = _case(cfg, seed=13)
+    y, ids, w, ws = _gpu_layer(cfg, inp)
+    ids2 = torch.full_like(ids, -5)
+    w2 = torch.full_like(w, float("nan"))
+    desc = moe.desc_from_config(cfg)
+    moe.moe_route(desc, inp["x"], inp["Wr"], inp["logit_bias"], inp["sel_bias"], ids2, w2, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    assert torch.equal(ids, ids2)
+    assert torch.equal(w, w2)
+    # a second layer call on the same workspace agrees bit for bit
+    y3 = torch.full_like(y, float("nan"))
+    ids3 = torch.full_like(ids, -7)
+    w3 = torch.empty_like(w)
+    moe.moe_layer_forward(desc, inp["x"], inp["Wr"], inp["logit_bias"], inp["sel_bias"],
+                          inp["Wg"], inp["Wu"], inp["Wd"], None, y3, ids3, w3, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    assert torch.equal(ids, ids3) and torch.equal(w, w3) and torch.equal(y, y3)
+
+
 # ---------------------------------------------------------------- whole layer, small
 # the largest shape the layer record admits: E=1024 routed + 4 shared experts
 # (1028 groups, the grouped GEMM's limit), top-32; softmax scores, whose gaps
