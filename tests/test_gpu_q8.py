@@ -113,3 +113,42 @@ def test_layer_forward_q8_full_size(cfg, n_sample):
                                  cfg.gate, S=cfg.S, tokens=tokens, **kw)
     got = host(y[torch.from_numpy(tokens).long().to(DEV)]).double().numpy()
     assert rel_err(got, y_ref) <= 1e-2, rel_err(got, y_ref)
+
+
+# Batch sizes on the tile edges of the Q8_0 kernels: 32-token tiles with
+# several issuers (mean batch <= 48 rows), and the large-batch variants
+# (192-token gate/up, 256-token down), with weight blocks that end inside a
+# matrix (I = 320, d = 192) and K of an odd number of 64-wide blocks (two-block
+# weight stages with a half-empty last stage).
+Q8_TILE_EDGE_CASES = [
+    ("small", LayerConfig("q8_edges_small", T=136, d=192, E=10, I=320, k=2),
+     [1, 15, 16, 17, 31, 32, 33, 63, 64, 0]),
+    ("large", LayerConfig("q8_edges_large", T=1498, d=192, E=12, I=320, k=2),
+     [1, 31, 33, 191, 192, 193, 255, 256, 257, 384, 500, 703]),
+]
+
+
+@pytest.mark.parametrize("name,cfg,sizes", Q8_TILE_EDGE_CASES,
+                         ids=[c[0] for c in Q8_TILE_EDGE_CASES])
+def test_expert_ffn_q8_tile_edges(name, cfg, sizes):
+    P = cfg.T * cfg.k
+    assert sum(sizes) == P and len(sizes) == cfg.E
+    inp = make_inputs(cfg, seed=29, device=DEV)
+    rng = np.random.default_rng(29)
+    off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int32)
+    tok = rng.integers(0, cfg.T, size=P).astype(np.int32)
+    desc = moe.desc_from_config(cfg)
+    ws = moe.alloc_workspace(desc)
+    Wg, Wu, Wd = (moe.quantize_q8_0(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    y_perm = torch.full((P, cfg.d), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.moe_expert_ffn_q8(desc, inp["x"], torch.from_numpy(off).to(DEV),
+                          torch.from_numpy(tok).to(DEV), None, Wg, Wu, Wd, y_perm, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    dg, du, dd = (_oracle_deq(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    got = host(y_perm).double().numpy()
+    for e in range(cfg.E):
+        if sizes[e] == 0:
+            continue
+        ref = oracle.expert_rows(host(inp["x"]), dg[e], du[e], dd[e], tok[off[e]:off[e + 1]])
+        err = rel_err(got[off[e]:off[e + 1]], ref)
+        assert err <= 1e-2, (e, sizes[e], err)
