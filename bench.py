@@ -300,12 +300,12 @@ def run_gpu(args, rank, world):
     moe.moe_profile_enable(False)
     stream = torch.cuda.current_stream()
 
-    # ---- end to end: pinned host x -> device, layer, device y -> pinned host
+    # ---- end to end: the C-ABI call with host buffers (moe_layer_forward_host):
+    # pinned host x -> device, layer, device y -> pinned host, every step
     x_host = x.cpu().pin_memory()
     y_host = torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory()
-    x_dev = torch.empty_like(x)
     for _ in range(max(1, args.warmup)):
-        layer.forward_host(x_host, y_host, x_dev, y, stream=stream)
+        layer.forward_host(x_host, y_host, stream=stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -313,7 +313,7 @@ def run_gpu(args, rank, world):
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     for _ in range(args.steps):
-        layer.forward_host(x_host, y_host, x_dev, y, stream=stream)
+        layer.forward_host(x_host, y_host, stream=stream)
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1)

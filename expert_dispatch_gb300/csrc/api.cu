@@ -59,6 +59,8 @@ struct Ws {
   void* x_perm;
   void* h;
   void* y_perm;
+  void* x_stage;
+  float* y_stage;
 };
 
 Ws carve(void* base, const WsLayout& L) {
@@ -80,6 +82,8 @@ Ws carve(void* base, const WsLayout& L) {
   w.x_perm = b + L.x_perm;
   w.h = b + L.h;
   w.y_perm = b + L.y_perm;
+  w.x_stage = b + L.x_stage;
+  w.y_stage = reinterpret_cast<float*>(b + L.y_stage);
   return w;
 }
 
@@ -251,6 +255,8 @@ WsLayout ws_layout(const moe_layer_desc& D) {
   L.x_perm = take(cap * (size_t)D.d * es);
   L.h = take(cap * (size_t)D.I * es);
   L.y_perm = take(P * (size_t)D.d * es);
+  L.x_stage = take(T * (size_t)D.d * es);
+  L.y_stage = take(T * (size_t)D.d * 4);
   L.total = off;
   return L;
 }
@@ -528,6 +534,65 @@ moe_status moe_layer_forward_q8(const moe_layer_desc* desc, const void* x, const
     return st;
   return cuda_status(launch_combine(desc->dtype, W.y_perm, W.slot_row, w, residual, desc->T,
                                     desc->d, desc->k, desc->S, y, s));
+}
+
+// The layer call with host buffers: x_host -> the workspace's x rows, the
+// layer on the device, its y rows -> y_host; all on `stream`.
+static moe_status forward_host_common(const moe_layer_desc* desc, const void* x_host,
+                                      float* y_host, void* workspace, size_t ws_bytes,
+                                      void* stream, const void** x_dev, float** y_dev) {
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
+  const Ws W = carve(workspace, ws_layout(*desc));
+  *x_dev = W.x_stage;
+  *y_dev = W.y_stage;
+  const size_t bytes = (size_t)desc->T * desc->d * dtype_size(desc->dtype);
+  return cuda_status(cudaMemcpyAsync(W.x_stage, x_host, bytes, cudaMemcpyHostToDevice,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+static moe_status copy_y_to_host(const moe_layer_desc* desc, const float* y_dev, float* y_host,
+                                 void* stream) {
+  return cuda_status(cudaMemcpyAsync(y_host, y_dev, (size_t)desc->T * desc->d * 4,
+                                     cudaMemcpyDeviceToHost, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_layer_forward_host(const moe_layer_desc* desc, const void* x_host,
+                                  const void* Wr, const float* logit_bias,
+                                  const float* sel_bias, const void* Wg, const void* Wu,
+                                  const void* Wd, const float* residual, float* y_host,
+                                  int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                                  size_t ws_bytes, void* stream) {
+  if (desc && desc->T == 0 && check_desc(desc) == MOE_OK) return MOE_OK;
+  const void* x = nullptr;
+  float* y = nullptr;
+  moe_status st = forward_host_common(desc, x_host, y_host, workspace, ws_bytes, stream, &x, &y);
+  if (st != MOE_OK) return st;
+  if ((st = moe_layer_forward(desc, x, Wr, logit_bias, sel_bias, Wg, Wu, Wd, residual, y,
+                              topk_ids_out, topk_w_out, workspace, ws_bytes, stream)) != MOE_OK)
+    return st;
+  return copy_y_to_host(desc, y, y_host, stream);
+}
+
+moe_status moe_layer_forward_q8_host(const moe_layer_desc* desc, const void* x_host,
+                                     const void* Wr, const float* logit_bias,
+                                     const float* sel_bias, const moe_q8_weight* Wg,
+                                     const moe_q8_weight* Wu, const moe_q8_weight* Wd,
+                                     const float* residual, float* y_host,
+                                     int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                                     size_t ws_bytes, void* stream) {
+  if (desc && desc->T == 0 && check_desc(desc) == MOE_OK) return MOE_OK;
+  const void* x = nullptr;
+  float* y = nullptr;
+  moe_status st = forward_host_common(desc, x_host, y_host, workspace, ws_bytes, stream, &x, &y);
+  if (st != MOE_OK) return st;
+  if ((st = moe_layer_forward_q8(desc, x, Wr, logit_bias, sel_bias, Wg, Wu, Wd, residual, y,
+                                 topk_ids_out, topk_w_out, workspace, ws_bytes, stream)) !=
+      MOE_OK)
+    return st;
+  return copy_y_to_host(desc, y, y_host, stream);
 }
 
 moe_status moe_combine_partial(const moe_layer_desc* desc, const void* y_perm,

@@ -43,7 +43,8 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_d
             "moe_slot_cache_destroy", "moe_slot_cache_assign", "moe_slot_cache_slot_of",
             "moe_slot_cache_get_stats", "moe_tier_create", "moe_tier_destroy",
             "moe_tier_prefetch", "moe_tier_forward", "moe_tier_get_stats", "moe_host_alloc",
-            "moe_host_free", "moe_check_bounded_wait")
+            "moe_host_free", "moe_check_bounded_wait", "moe_layer_forward_host",
+            "moe_layer_forward_q8_host")
 
 
 class MoeError(RuntimeError):
@@ -121,6 +122,9 @@ def lib():
     L.moe_quantize_q8_0.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
     L.moe_expert_ffn_q8.argtypes = [D, vp, vp, vp, vp, Q, Q, Q, vp, vp, sz, vp]
     L.moe_layer_forward_q8.argtypes = [D, vp, vp, vp, vp, Q, Q, Q, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_layer_forward_host.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.moe_layer_forward_q8_host.argtypes = [D, vp, vp, vp, vp, Q, Q, Q, vp, vp, vp, vp, vp, sz,
+                                            vp]
     vpp = ctypes.POINTER(ctypes.c_void_p)
     ip = ctypes.POINTER(ctypes.c_int32)
     TS = ctypes.POINTER(TierStats)
@@ -609,12 +613,33 @@ class MoeLayer:
             topk_ids, topk_w, self.ws, stream)
         return y
 
-    def forward_host(self, x_host, y_host, x_dev, y_dev, stream=None):
-        """End-to-end call with host buffers: pinned x_host -> device, the layer,
-        device y -> pinned y_host (all on one stream, asynchronous)."""
-        s = stream if stream is not None else torch.cuda.current_stream()
-        with torch.cuda.stream(s):
-            x_dev.copy_(x_host, non_blocking=True)
-            self.forward(x_dev, y=y_dev, stream=s)
-            y_host.copy_(y_dev, non_blocking=True)
+    def forward_host(self, x_host, y_host, residual=None, stream=None):
+        """The layer call with host buffers (moe_layer_forward_host): x_host and
+        y_host are CPU tensors (page-locked for asynchronous copies); the library
+        copies x in, runs the layer and copies y out, all on the stream."""
+        d = self.desc
+        _need(x_host, (d.T, d.d), "x_host")
+        _need(y_host, (d.T, d.d), "y_host")
+        if x_host.is_cuda or y_host.is_cuda:
+            raise ValueError("forward_host takes host (CPU) tensors")
+        if x_host.dtype != _act_dtype(d) or y_host.dtype != torch.float32:
+            raise TypeError("x_host must be %s and y_host float32" % _act_dtype(d))
+        if not (x_host.is_contiguous() and y_host.is_contiguous()):
+            raise ValueError("forward_host takes contiguous host tensors")
+        common = (ctypes.byref(d), ctypes.c_void_p(x_host.data_ptr()),
+                  _p(self.Wr, None, "Wr"), _p(self.logit_bias, torch.float32, "logit_bias"),
+                  _p(self.sel_bias, torch.float32, "sel_bias"))
+        tail = (_p(residual, torch.float32, "residual"), ctypes.c_void_p(y_host.data_ptr()),
+                None, None, _p(self.ws, torch.uint8, "workspace"), self.ws.numel(),
+                _stream(stream))
+        if self.q8:
+            g, u, w = self.Wg.struct(), self.Wu.struct(), self.Wd.struct()
+            st = lib().moe_layer_forward_q8_host(*common, ctypes.byref(g), ctypes.byref(u),
+                                                 ctypes.byref(w), *tail)
+            _check(st, "moe_layer_forward_q8_host")
+        else:
+            st = lib().moe_layer_forward_host(*common, _p(self.Wg, None, "Wg"),
+                                              _p(self.Wu, None, "Wu"), _p(self.Wd, None, "Wd"),
+                                              *tail)
+            _check(st, "moe_layer_forward_host")
         return y_host

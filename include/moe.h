@@ -343,6 +343,29 @@ moe_status moe_tier_forward(moe_expert_tier* tier, const moe_layer_desc* desc, c
                             float* topk_w_out, void* workspace, size_t ws_bytes, void* stream);
 moe_status moe_tier_get_stats(moe_expert_tier* tier, moe_tier_stats* out);
 
+/* The layer call with host buffers (the pages' forward RPC, its input and
+   output on the host side): x_host ([T, d], the layer's dtype) is copied into
+   the workspace, the layer runs exactly as moe_layer_forward (or
+   moe_layer_forward_q8) on it, and y ([T, d] fp32) is copied to y_host; all
+   enqueued on `stream`, asynchronously, so y_host holds the result once the
+   stream has passed the call (page-locked host buffers make the copies
+   asynchronous).  The other pointers (weights, biases, residual, top-k
+   outputs) are device memory as for moe_layer_forward.  Errors as
+   moe_layer_forward; MOE_ERR_INVALID_ARG for a NULL host buffer. */
+moe_status moe_layer_forward_host(const moe_layer_desc* desc, const void* x_host,
+                                  const void* Wr, const float* logit_bias,
+                                  const float* sel_bias, const void* Wg, const void* Wu,
+                                  const void* Wd, const float* residual, float* y_host,
+                                  int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                                  size_t ws_bytes, void* stream);
+moe_status moe_layer_forward_q8_host(const moe_layer_desc* desc, const void* x_host,
+                                     const void* Wr, const float* logit_bias,
+                                     const float* sel_bias, const moe_q8_weight* Wg,
+                                     const moe_q8_weight* Wu, const moe_q8_weight* Wd,
+                                     const float* residual, float* y_host,
+                                     int32_t* topk_ids_out, float* topk_w_out, void* workspace,
+                                     size_t ws_bytes, void* stream);
+
 /* Synchronizes `stream`, then reports the sticky device flag held in the
    workspace: MOE_OK, MOE_ERR_DEVICE_INPUT or MOE_ERR_TIMEOUT (MOE_ERR_CUDA if
    the copy itself fails).  clear != 0 resets the flag afterwards.          */

@@ -288,6 +288,23 @@ def test_layer_routing_matches_router_call_and_repeats(cfg):
     assert torch.equal(ids, ids3) and torch.equal(w, w3) and torch.equal(y, y3)
 
 
+# The layer call with host buffers equals the device call bit for bit.
+@pytest.mark.parametrize("cfg", [FFN_CASES[0], FFN_CASES[5], FFN_CASES[6]],
+                         ids=lambda c: c.name)
+def test_layer_forward_host_buffers(cfg):
+    inp = _case(cfg, seed=17)
+    desc = moe.desc_from_config(cfg)
+    layer = moe.MoeLayer(desc, inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"],
+                         logit_bias=inp["logit_bias"], sel_bias=inp["sel_bias"])
+    y_dev = layer.forward(inp["x"])
+    x_host = host(inp["x"]).pin_memory()
+    y_host = torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.float32).pin_memory()
+    layer.forward_host(x_host, y_host)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
+    assert torch.equal(y_host, host(y_dev))
+
+
 # ---------------------------------------------------------------- whole layer, small
 # the largest shape the layer record admits: E=1024 routed + 4 shared experts
 # (1028 groups, the grouped GEMM's limit), top-32; softmax scores, whose gaps

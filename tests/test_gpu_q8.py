@@ -152,3 +152,19 @@ def test_expert_ffn_q8_tile_edges(name, cfg, sizes):
         ref = oracle.expert_rows(host(inp["x"]), dg[e], du[e], dd[e], tok[off[e]:off[e + 1]])
         err = rel_err(got[off[e]:off[e + 1]], ref)
         assert err <= 1e-2, (e, sizes[e], err)
+
+
+def test_layer_forward_q8_host_buffers():
+    cfg = Q8_CASES[0]
+    inp = enforce_margins(make_inputs(cfg, seed=31, device=DEV), cfg, 31)
+    desc = moe.desc_from_config(cfg)
+    Wg, Wu, Wd = (moe.quantize_q8_0(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    layer = moe.MoeLayer(desc, inp["Wr"], Wg, Wu, Wd, logit_bias=inp["logit_bias"],
+                         sel_bias=inp["sel_bias"])
+    y_dev = layer.forward(inp["x"])
+    x_host = host(inp["x"]).pin_memory()
+    y_host = torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.float32).pin_memory()
+    layer.forward_host(x_host, y_host)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
+    assert torch.equal(y_host, host(y_dev))
