@@ -331,6 +331,40 @@ def test_layer_forward_parity_small(cfg):
     assert rel_err(moe_part, moe_ref) <= y_tol(cfg), rel_err(moe_part, moe_ref)
 
 
+# Seeded random tiny shapes across the whole layer (both dtypes, both gate
+# families, with and without a shared expert): T in 1..67, E in 4..40, k in
+# 1..min(E, 8); d and I multiples of 64 (bf16) or of 8 / 4 (fp32).
+def _random_tiny_config(seed):
+    rng = np.random.default_rng(1000 + seed)
+    f32 = seed % 3 == 0
+    E = int(rng.integers(4, 41))
+    k = int(rng.integers(1, min(E, 8) + 1))
+    S = int(rng.integers(0, 2))
+    gate = int(rng.integers(0, 2))
+    if f32:
+        d, I = 8 * int(rng.integers(2, 33)), 4 * int(rng.integers(2, 65))
+    else:
+        d, I = 64 * int(rng.integers(1, 5)), 64 * int(rng.integers(1, 5))
+        while (E + S) * min(d, I) < 128:
+            d, I = d + 64, I + 64
+    return LayerConfig("tiny_%d" % seed, T=int(rng.integers(1, 68)), d=d, E=E, I=I, k=k, S=S,
+                       gate=gate, norm_topk=gate, routed_scaling=2.0 if gate else 1.0,
+                       sel_bias_range=0.1 if gate else 0.0, dtype="f32" if f32 else "bf16")
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_layer_forward_random_tiny_shapes(seed):
+    cfg = _random_tiny_config(seed)
+    inp = _case(cfg, seed=seed)
+    y, ids, w, _ = _gpu_layer(cfg, inp)
+    ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
+                                  **_oracle_kw(cfg, inp))
+    np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
+    np.testing.assert_allclose(host(w).numpy(), w_ref, rtol=W_RTOL, atol=0)
+    y_ref, _, _ = _oracle_forward(cfg, inp, np.arange(cfg.T, dtype=np.int32), ids_ref)
+    assert rel_err(host(y).double().numpy(), y_ref) <= y_tol(cfg), (cfg, rel_err(host(y).double().numpy(), y_ref))
+
+
 def test_layer_forward_with_no_tokens_is_a_no_op():
     cfg = FFN_CASES[4]
     inp = _case(cfg, seed=2)
