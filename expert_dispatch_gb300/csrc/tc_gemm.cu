@@ -29,6 +29,10 @@
 //     tiles are requested before waiting for the previous kernel.
 //   * Every wait is bounded (1 s); on expiry the CTA records a timeout in the
 //     error word, drains its own copies and MMAs, frees TMEM and exits.
+// Variants here: 32-token tiles (decode-sized batches, both FFN GEMMs),
+// 256-token gate/up tiles (the largest batches) and the router.  The other
+// large-batch FFN GEMMs run on SM pairs (tc_gemm_pair.cu); launch_ffn_tc
+// picks per GEMM.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
