@@ -78,6 +78,10 @@ ROUTER_CASES = [
                 routed_scaling=2.827, sel_bias_range=0.1),
     # CUDA-core router over several token runs per expert row (the last one ragged)
     LayerConfig("r_bf16_simt_runs", T=600, d=320, E=40, I=64, k=4),
+    # every expert selected (k = E): the weights are the whole softmax / the normalised scores
+    LayerConfig("r_k_equals_E_softmax", T=33, d=128, E=8, I=64, k=8),
+    LayerConfig("r_k_equals_E_sigmoid", T=33, d=128, E=8, I=64, k=8, S=1, gate=1, norm_topk=1,
+                routed_scaling=2.5, sel_bias_range=0.1),
 ]
 
 
@@ -310,7 +314,8 @@ def test_layer_forward_host_buffers(cfg):
 # (1028 groups, the grouped GEMM's limit), top-32; softmax scores, whose gaps
 # among the top 33 of 1024 stay wide enough for the routing margin
 MAX_GROUPS = LayerConfig("l_max_groups", T=40, d=128, E=1024, I=64, k=32, S=4, norm_topk=1)
-LAYER_CASES = FFN_CASES + [ROUTER_CASES[2], ROUTER_CASES[3], MAX_GROUPS]
+LAYER_CASES = FFN_CASES + [ROUTER_CASES[2], ROUTER_CASES[3], MAX_GROUPS] + [
+    c for c in ROUTER_CASES if c.name.startswith("r_k_equals_E")]
 
 
 @pytest.mark.parametrize("cfg", LAYER_CASES, ids=lambda c: c.name)
@@ -338,7 +343,7 @@ def _random_tiny_config(seed):
     rng = np.random.default_rng(1000 + seed)
     f32 = seed % 3 == 0
     E = int(rng.integers(4, 41))
-    k = int(rng.integers(1, min(E, 8) + 1))
+    k = int(rng.integers(1, min(E, 32) + 1))  # the library's whole k range
     S = int(rng.integers(0, 2))
     gate = int(rng.integers(0, 2))
     if f32:
@@ -352,7 +357,7 @@ def _random_tiny_config(seed):
                        sel_bias_range=0.1 if gate else 0.0, dtype="f32" if f32 else "bf16")
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(16))
 def test_layer_forward_random_tiny_shapes(seed):
     cfg = _random_tiny_config(seed)
     inp = _case(cfg, seed=seed)
