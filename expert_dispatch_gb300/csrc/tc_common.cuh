@@ -188,7 +188,9 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, i
 // the first ones.
 //
 // Units u0, u0 + ustride, ... are this CTA's; a unit's weight block covers
-// rows mt * MT + row_off .. + 127 of the group.  With PAIR the accumulator
+// rows mt * MT + row_off .. + 127 of the group, or, for MODE_DOWN with two
+// accumulators (MT = 256 on one SM), rows mt * 256 .. + 255: the first
+// accumulator holds the upper 128, the second the lower.  With PAIR the accumulator
 // buffers are released on the even CTA of the cluster (the pair's MMA
 // issuer), whatever CTA this is.
 template <int MODE, int BN, int NACC, int NBUF, bool H_F16 = false, int NPART = 1, int MT = 128,
@@ -256,6 +258,52 @@ __device__ __forceinline__ void epilogue_loop(const Params& p, int total, int m_
       tc_fence_before();
       __syncwarp();
       if (lane == 0) release(buf);
+    } else if constexpr (MODE == MODE_DOWN && NACC == 2) {
+      // Two stacked 128-row weight blocks (a unit of MT = 256 rows): warps
+      // 0-3 of the epilogue take the first accumulator, 4-7 the second, each
+      // over all of the tile's columns.
+      static_assert(NPART == 1 && !PAIR && MT == 256, "stacked down accumulators");
+      constexpr int NC2 = BN / 16;
+      const int m2 = t.mt * MT + row_off + half * 128 + q * 32 + lane;
+      const uint32_t ta = tb + (uint32_t)(half * BN);
+      uint32_t a[NC2][16];
+#pragma unroll
+      for (int i = 0; i < NC2; ++i)
+        if (16 * i < t.nt) tmem_ld16(ta + 16 * i, a[i]);  // warp-uniform
+      tmem_ld_wait();
+      uint32_t pk[NC2][8];
+#pragma unroll
+      for (int i = 0; i < NC2; ++i) {
+        const int c0 = 16 * i;
+        if (c0 >= t.nt) break;  // warp-uniform: the chunks that were loaded
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          float v0 = __uint_as_float(a[i][j]), v1 = __uint_as_float(a[i][j + 1]);
+          if (p.row_scale) {  // read for batch rows only
+            if (c0 + j < t.nt) v0 *= p.row_scale[t.r0 + c0 + j];
+            if (c0 + j + 1 < t.nt) v1 *= p.row_scale[t.r0 + c0 + j + 1];
+          }
+          const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+          pk[i][j / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) release(buf);  // TMEM free: stores follow
+      if (m2 < p.Mg) {
+        uint16_t* out = static_cast<uint16_t*>(p.out);
+#pragma unroll
+        for (int i = 0; i < NC2; ++i) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int col = 16 * i + j;
+            if (col >= t.nt) break;
+            const uint32_t w = pk[i][j / 2];
+            out[(size_t)(t.r0 + col) * p.ldo + m2] =
+                (uint16_t)((j & 1) ? (w >> 16) : (w & 0xffffu));
+          }
+        }
+      }
     } else {
       uint32_t pk[NCH][8];  // the unit's results, packed 16-bit pairs
 #pragma unroll

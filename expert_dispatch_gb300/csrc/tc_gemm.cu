@@ -52,9 +52,13 @@ using tc::Params;
 using tc::Unit;
 constexpr int kThreads = 32 * (2 + tc::kEpiWarps);  // producer, MMA, epilogue
 
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int STAGES, int MT = 128>
 struct Cfg {
-  static constexpr int NA = MODE == MODE_GATEUP ? 2 : 1;  // weight operands per stage
+  // weight operands per stage: gate and up, or two 128-row blocks of one
+  // matrix when a unit spans MT = 256 weight rows
+  static constexpr int NA = MODE == MODE_GATEUP || MT == 256 ? 2 : 1;
+  // the second operand's first row, relative to the unit's
+  static constexpr int A1_ROW = MODE == MODE_GATEUP ? 0 : 128;
   static constexpr int A_BYTES = 128 * 64 * 2;
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
@@ -70,17 +74,18 @@ struct Cfg {
   static constexpr int GSTART_OFF = PREFIX_OFF + 4 * (tc::kMaxGroups + 1);
   static constexpr int SMEM_TOTAL = GSTART_OFF + 4 * (tc::kMaxGroups + 1) + 1024;
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "token tile");
+  static_assert(MT == 128 || (MT == 256 && MODE != MODE_GATEUP), "weight rows per unit");
   static_assert(COLS <= 512, "TMEM columns");
   static_assert(SMEM_TOTAL <= 232448, "shared memory");
 };
 
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int STAGES, int MT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA0,
                     const __grid_constant__ CUtensorMap tmA1,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmBfull, const Params p) {
-  using C = Cfg<MODE, BN, STAGES>;
+  using C = Cfg<MODE, BN, STAGES, MT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -97,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* gstart = reinterpret_cast<int*>(smem + C::GSTART_OFF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tiles = (p.Mg + 127) / 128;
+  const int m_tiles = (p.Mg + MT - 1) / MT;
   const int KB = p.K / 64;
 
   if (threadIdx.x == 0) {
@@ -142,14 +147,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit t =
             tc::decode_unit<MODE, BN>(blockIdx.x, prefix, gstart, p.n_groups, m_tiles, KB, p);
         const uint32_t bytes = C::NA * C::A_BYTES + ((t.nt + 31) / 32) * 4096;
-        const int arow = tc::weight_mat(p, t.g) * p.Mg + t.mt * 128;
+        const int arow = tc::weight_mat(p, t.g) * p.Mg + t.mt * MT;
         n_pre = min(STAGES, t.kb1 - t.kb0);
         for (int i = 0; i < n_pre; ++i) {  // fresh ring: stages 0..n_pre-1 are free
           mbar_arrive_expect_tx(full_bar(i), bytes);
           armed |= 1u << i;
           const uint32_t sA = sbase + i * C::STAGE_BYTES;
           tma_load_2d(sA, &tmA0, full_bar(i), (t.kb0 + i) * 64, arow);
-          if (C::NA == 2) tma_load_2d(sA + C::A_BYTES, &tmA1, full_bar(i), (t.kb0 + i) * 64, arow);
+          if (C::NA == 2)
+            tma_load_2d(sA + C::A_BYTES, &tmA1, full_bar(i), (t.kb0 + i) * 64, arow + C::A1_ROW);
         }
       }
       pdl_wait();
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Unit t = tc::decode_unit<MODE, BN>(u, prefix, gstart, p.n_groups, m_tiles, KB, p);
         const int nchunks = (t.nt + 31) / 32;
         const uint32_t bytes = C::NA * C::A_BYTES + nchunks * 4096;
-        const int arow = tc::weight_mat(p, t.g) * p.Mg + t.mt * 128;
+        const int arow = tc::weight_mat(p, t.g) * p.Mg + t.mt * MT;
         bool ok = true;
         for (int kb = t.kb0; kb < t.kb1; ++kb) {
           const bool pre = first && kb - t.kb0 < n_pre;  // armed, weights already requested
@@ -175,7 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sA = sbase + stage * C::STAGE_BYTES;
           if (!pre) {
             tma_load_2d(sA, &tmA0, full_bar(stage), kb * 64, arow);
-            if (C::NA == 2) tma_load_2d(sA + C::A_BYTES, &tmA1, full_bar(stage), kb * 64, arow);
+            if (C::NA == 2)
+              tma_load_2d(sA + C::A_BYTES, &tmA1, full_bar(stage), kb * 64, arow + C::A1_ROW);
           }
           const uint32_t sB = sA + C::NA * C::A_BYTES;
           if (t.nt == BN)  // a full token tile: one box of BN rows
@@ -246,9 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..9)
-    tc::epilogue_loop<MODE, BN, C::NACC, C::NBUF>(p, total, m_tiles, KB, prefix, gstart,
-                                                  tmem_base, accf0, acce0, abort_flag, 2,
-                                                  blockIdx.x, gridDim.x, 0);
+    tc::epilogue_loop<MODE, BN, C::NACC, C::NBUF, false, 1, MT>(
+        p, total, m_tiles, KB, prefix, gstart, tmem_base, accf0, acce0, abort_flag, 2, blockIdx.x,
+        gridDim.x, 0);
   }
 
   tc_fence_before();
@@ -287,12 +294,12 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t rows,
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int MODE, int BN, int STAGES>
+template <int MODE, int BN, int STAGES, int MT = 128>
 cudaError_t launch_tc(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                       const CUtensorMap& bfull, const Params& p, long long max_units,
                       const char* name, cudaStream_t s) {
-  using C = Cfg<MODE, BN, STAGES>;
-  auto kern = tc_grouped_gemm<MODE, BN, STAGES>;
+  using C = Cfg<MODE, BN, STAGES, MT>;
+  auto kern = tc_grouped_gemm<MODE, BN, STAGES, MT>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -364,8 +371,10 @@ cudaError_t launch_ffn_tc(const void* x_perm, const int32_t* offsets, int n_grou
     const cudaError_t e = launch_tc<MODE_GATEUP, 32, 6>(tg, tu, tx, tx, p1, (I + 127) / 128 * tiles,
                                                         "ffn_gateup_tc", s);
     if (e != cudaSuccess) return e;
-    return launch_tc<MODE_DOWN, 32, 10>(td, td, th, th, p2, (d + 127) / 128 * tiles, "ffn_down_tc",
-                                        s);
+    // down: units of 256 weight rows (two 128-row blocks per stage, as gate/up's
+    // two matrices), so each stage carries 32 KB of weights
+    return launch_tc<MODE_DOWN, 32, 6, 256>(td, td, th, th, p2, (d + 255) / 256 * tiles,
+                                            "ffn_down_tc", s);
   }
   // SM pairs: one token box per CTA and K block, (i + 1) * 16 rows high
   PairTokenMaps pxm, phm;
