@@ -300,20 +300,26 @@ def run_gpu(args, rank, world):
     moe.moe_profile_enable(False)
     stream = torch.cuda.current_stream()
 
-    # ---- end to end: the C-ABI call with host buffers (moe_layer_forward_host):
-    # pinned host x -> device, layer, device y -> pinned host, every step
-    x_host = x.cpu().pin_memory()
-    y_host = torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory()
-    for _ in range(max(1, args.warmup)):
-        layer.forward_host(x_host, y_host, stream=stream)
+    # ---- end to end: the C-ABI call a serving loop makes with host buffers
+    # (moe_layer_forward_host_pipelined): every step, pinned host x -> device,
+    # the layer, device y -> pinned host; the copies of neighbouring steps overlap
+    # the compute.  Two pinned x and two pinned y buffers, used in turn.
+    x_ring = [x.cpu().pin_memory() for _ in range(2)]
+    y_ring = [torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory() for _ in range(2)]
+    x_host, y_host = x_ring[0], y_ring[0]
+
+    def host_run(n):
+        layer.forward_host_pipelined([x_ring[i % 2] for i in range(n)],
+                                     [y_ring[i % 2] for i in range(n)], stream=stream)
+
+    host_run(max(1, args.warmup))
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for _ in range(args.steps):
-        layer.forward_host(x_host, y_host, stream=stream)
+    host_run(args.steps)
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1)
@@ -355,7 +361,9 @@ def run_gpu(args, rank, world):
         "kernels": per_kernel,
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
-                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
+                "call": "moe_layer_forward%s_host_pipelined, %d steps in one call"
+                        % ("_q8" if args.weights == "q8_0" else "", args.steps)},
         "gpu_launches": launches,
         "launch_mode": "cuda_graph_replay" if graph is not None else "direct",
         "kernel_timing": "event pair per launch over %d directly launched steps" % args.steps,

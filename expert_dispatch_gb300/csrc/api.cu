@@ -70,8 +70,8 @@ struct Ws {
   void* x_perm;
   void* h;
   void* y_perm;
-  void* x_stage;
-  float* y_stage;
+  void* x_stage[2];
+  float* y_stage[2];
 };
 
 Ws carve(void* base, const WsLayout& L) {
@@ -93,8 +93,10 @@ Ws carve(void* base, const WsLayout& L) {
   w.x_perm = b + L.x_perm;
   w.h = b + L.h;
   w.y_perm = b + L.y_perm;
-  w.x_stage = b + L.x_stage;
-  w.y_stage = reinterpret_cast<float*>(b + L.y_stage);
+  for (int i = 0; i < 2; ++i) {
+    w.x_stage[i] = b + L.x_stage[i];
+    w.y_stage[i] = reinterpret_cast<float*>(b + L.y_stage[i]);
+  }
   return w;
 }
 
@@ -266,8 +268,10 @@ WsLayout ws_layout(const moe_layer_desc& D) {
   L.x_perm = take(cap * (size_t)D.d * es);
   L.h = take(cap * (size_t)D.I * es);
   L.y_perm = take(P * (size_t)D.d * es);
-  L.x_stage = take(T * (size_t)D.d * es);
-  L.y_stage = take(T * (size_t)D.d * 4);
+  for (int i = 0; i < 2; ++i) {
+    L.x_stage[i] = take(T * (size_t)D.d * es);
+    L.y_stage[i] = take(T * (size_t)D.d * 4);
+  }
   L.total = off;
   return L;
 }
@@ -406,6 +410,96 @@ moe_status tier_load(moe_expert_tier* t, int e, int slot, cudaStream_t s) {
   }
   t->bytes_loaded += 3 * t->mat_bytes;
   return MOE_OK;
+}
+
+
+// A run of layer calls on host buffers with the copies off the compute stream.
+// Step i computes from x stage i % 2 into y stage i % 2 on `stream`; an upload
+// stream brings x_host[i + 1] into the other x stage while step i computes, and
+// a download stream takes y stage i to y_host[i] while step i + 1 computes.
+// Events order the three streams:
+//   upload i + 1   after  step i - 1 (its x stage was read there)
+//   step i         after  upload i, and after download i - 2 (its y stage)
+//   download i     after  step i
+// The run begins after the work on `stream` before the call (both copy
+// streams wait for it) and `stream` waits for the last download, so work
+// enqueued after the call sees every y_host[i] written.  The copy streams and
+// events are the call's own and are released once their work completes.
+struct PipelineRes {
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaEvent_t start = nullptr, x_ready[2] = {}, computed[2] = {}, y_done[2] = {};
+  ~PipelineRes() {
+    cudaEvent_t* evs[] = {&start, &x_ready[0], &x_ready[1], &computed[0], &computed[1],
+                          &y_done[0], &y_done[1]};
+    for (cudaEvent_t* e : evs)
+      if (*e) cudaEventDestroy(*e);
+    if (up) cudaStreamDestroy(up);
+    if (down) cudaStreamDestroy(down);
+  }
+  bool create() {
+    if (cudaStreamCreateWithFlags(&up, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&down, cudaStreamNonBlocking) != cudaSuccess)
+      return false;
+    cudaEvent_t* evs[] = {&start, &x_ready[0], &x_ready[1], &computed[0], &computed[1],
+                          &y_done[0], &y_done[1]};
+    for (cudaEvent_t* e : evs)
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
+    return true;
+  }
+};
+
+template <typename LayerFn>
+moe_status forward_host_pipelined(const moe_layer_desc* desc, int n_steps,
+                                  const void* const* x_host, float* const* y_host,
+                                  void* workspace, size_t ws_bytes, void* stream,
+                                  const LayerFn& layer) {
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (n_steps < 0) return MOE_ERR_INVALID_ARG;
+  if (n_steps == 0 || desc->T == 0) return MOE_OK;
+  if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n_steps; ++i)
+    if (!x_host[i] || !y_host[i]) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
+  const Ws W = carve(workspace, ws_layout(*desc));
+  const size_t xb = (size_t)desc->T * desc->d * dtype_size(desc->dtype);
+  const size_t yb = (size_t)desc->T * desc->d * 4;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PipelineRes R;
+  if (!R.create()) return MOE_ERR_CUDA;
+  bool ok = cudaEventRecord(R.start, s) == cudaSuccess &&
+            cudaStreamWaitEvent(R.up, R.start, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(R.down, R.start, 0) == cudaSuccess;
+  auto upload = [&](int i) {
+    const int b = i & 1;
+    return (i < 2 || cudaStreamWaitEvent(R.up, R.computed[b], 0) == cudaSuccess) &&
+           cudaMemcpyAsync(W.x_stage[b], x_host[i], xb, cudaMemcpyHostToDevice, R.up) ==
+               cudaSuccess &&
+           cudaEventRecord(R.x_ready[b], R.up) == cudaSuccess;
+  };
+  ok = ok && upload(0);
+  for (int i = 0; ok && i < n_steps; ++i) {
+    const int b = i & 1;
+    if (i + 1 < n_steps && !(ok = upload(i + 1))) break;
+    if (cudaStreamWaitEvent(s, R.x_ready[b], 0) != cudaSuccess ||
+        (i >= 2 && cudaStreamWaitEvent(s, R.y_done[b], 0) != cudaSuccess)) {
+      ok = false;
+      break;
+    }
+    if ((st = layer(W.x_stage[b], W.y_stage[b])) != MOE_OK) break;
+    ok = cudaEventRecord(R.computed[b], s) == cudaSuccess &&
+         cudaStreamWaitEvent(R.down, R.computed[b], 0) == cudaSuccess &&
+         cudaMemcpyAsync(y_host[i], W.y_stage[b], yb, cudaMemcpyDeviceToHost, R.down) ==
+             cudaSuccess &&
+         cudaEventRecord(R.y_done[b], R.down) == cudaSuccess;
+  }
+  // join: whatever was enqueued on the copy streams ends before later work on `stream`
+  const bool joined = cudaEventRecord(R.x_ready[0], R.up) == cudaSuccess &&
+                      cudaEventRecord(R.y_done[0], R.down) == cudaSuccess &&
+                      cudaStreamWaitEvent(s, R.x_ready[0], 0) == cudaSuccess &&
+                      cudaStreamWaitEvent(s, R.y_done[0], 0) == cudaSuccess;
+  if (st != MOE_OK) return st;
+  return ok && joined ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
@@ -564,10 +658,10 @@ static moe_status forward_host_common(const moe_layer_desc* desc, const void* x_
   if (!x_host || !y_host) return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(desc, workspace, ws_bytes)) != MOE_OK) return st;
   const Ws W = carve(workspace, ws_layout(*desc));
-  *x_dev = W.x_stage;
-  *y_dev = W.y_stage;
+  *x_dev = W.x_stage[0];
+  *y_dev = W.y_stage[0];
   const size_t bytes = (size_t)desc->T * desc->d * dtype_size(desc->dtype);
-  return cuda_status(cudaMemcpyAsync(W.x_stage, x_host, bytes, cudaMemcpyHostToDevice,
+  return cuda_status(cudaMemcpyAsync(W.x_stage[0], x_host, bytes, cudaMemcpyHostToDevice,
                                      static_cast<cudaStream_t>(stream)));
 }
 
@@ -613,6 +707,36 @@ moe_status moe_layer_forward_q8_host(const moe_layer_desc* desc, const void* x_h
       MOE_OK)
     return st;
   return copy_y_to_host(desc, y, y_host, stream);
+}
+
+moe_status moe_layer_forward_host_pipelined(const moe_layer_desc* desc, int n_steps,
+                                            const void* const* x_host, const void* Wr,
+                                            const float* logit_bias, const float* sel_bias,
+                                            const void* Wg, const void* Wu, const void* Wd,
+                                            float* const* y_host, void* workspace,
+                                            size_t ws_bytes, void* stream) {
+  const NvtxRange nvtx("moe_layer_forward_host_pipelined");
+  return forward_host_pipelined(
+      desc, n_steps, x_host, y_host, workspace, ws_bytes, stream,
+      [&](const void* x, float* y) {
+        return moe_layer_forward(desc, x, Wr, logit_bias, sel_bias, Wg, Wu, Wd, nullptr, y,
+                                 nullptr, nullptr, workspace, ws_bytes, stream);
+      });
+}
+
+moe_status moe_layer_forward_q8_host_pipelined(const moe_layer_desc* desc, int n_steps,
+                                               const void* const* x_host, const void* Wr,
+                                               const float* logit_bias, const float* sel_bias,
+                                               const moe_q8_weight* Wg, const moe_q8_weight* Wu,
+                                               const moe_q8_weight* Wd, float* const* y_host,
+                                               void* workspace, size_t ws_bytes, void* stream) {
+  const NvtxRange nvtx("moe_layer_forward_q8_host_pipelined");
+  return forward_host_pipelined(
+      desc, n_steps, x_host, y_host, workspace, ws_bytes, stream,
+      [&](const void* x, float* y) {
+        return moe_layer_forward_q8(desc, x, Wr, logit_bias, sel_bias, Wg, Wu, Wd, nullptr, y,
+                                    nullptr, nullptr, workspace, ws_bytes, stream);
+      });
 }
 
 moe_status moe_combine_partial(const moe_layer_desc* desc, const void* y_perm,

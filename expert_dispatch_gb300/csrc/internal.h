@@ -30,8 +30,8 @@ struct WsLayout {
   size_t x_perm;       // dtype [cap, d], cap = tc_row_capacity(P)
   size_t h;            // dtype [cap, I]
   size_t y_perm;       // dtype [P, d]
-  size_t x_stage;      // dtype [T, d]: x of a call with host buffers
-  size_t y_stage;      // fp32 [T, d]:  y of a call with host buffers
+  size_t x_stage[2];   // dtype [T, d]: x of a call with host buffers (two: pipelined call)
+  size_t y_stage[2];   // fp32 [T, d]:  y of a call with host buffers (two: pipelined call)
   size_t total;
 };
 

@@ -44,7 +44,8 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_d
             "moe_slot_cache_get_stats", "moe_tier_create", "moe_tier_destroy",
             "moe_tier_prefetch", "moe_tier_forward", "moe_tier_get_stats", "moe_host_alloc",
             "moe_host_free", "moe_check_bounded_wait", "moe_layer_forward_host",
-            "moe_layer_forward_q8_host")
+            "moe_layer_forward_q8_host", "moe_layer_forward_host_pipelined",
+            "moe_layer_forward_q8_host_pipelined")
 
 
 class MoeError(RuntimeError):
@@ -125,6 +126,10 @@ def lib():
     L.moe_layer_forward_host.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.moe_layer_forward_q8_host.argtypes = [D, vp, vp, vp, vp, Q, Q, Q, vp, vp, vp, vp, vp, sz,
                                             vp]
+    L.moe_layer_forward_host_pipelined.argtypes = [D, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                                   vp]
+    L.moe_layer_forward_q8_host_pipelined.argtypes = [D, i32, vp, vp, vp, vp, Q, Q, Q, vp, vp, sz,
+                                                      vp]
     vpp = ctypes.POINTER(ctypes.c_void_p)
     ip = ctypes.POINTER(ctypes.c_int32)
     TS = ctypes.POINTER(TierStats)
@@ -643,3 +648,41 @@ class MoeLayer:
                                               *tail)
             _check(st, "moe_layer_forward_host")
         return y_host
+
+    def forward_host_pipelined(self, x_hosts, y_hosts, stream=None):
+        """A run of layer calls on host buffers with the copies overlapped
+        (moe_layer_forward_host_pipelined): step i reads x_hosts[i] and writes
+        y_hosts[i] (CPU tensors, page-locked for asynchronous copies); no
+        residual.  The run is ordered on the stream like a single call."""
+        d = self.desc
+        if len(x_hosts) != len(y_hosts):
+            raise ValueError("one output buffer per input buffer")
+        for x_host, y_host in zip(x_hosts, y_hosts):
+            _need(x_host, (d.T, d.d), "x_host")
+            _need(y_host, (d.T, d.d), "y_host")
+            if x_host.is_cuda or y_host.is_cuda:
+                raise ValueError("forward_host_pipelined takes host (CPU) tensors")
+            if x_host.dtype != _act_dtype(d) or y_host.dtype != torch.float32:
+                raise TypeError("x_host must be %s and y_host float32" % _act_dtype(d))
+            if not (x_host.is_contiguous() and y_host.is_contiguous()):
+                raise ValueError("forward_host_pipelined takes contiguous host tensors")
+        n = len(x_hosts)
+        xs = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in x_hosts])
+        ys = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in y_hosts])
+        head = (ctypes.byref(d), n, ctypes.cast(xs, ctypes.c_void_p), _p(self.Wr, None, "Wr"),
+                _p(self.logit_bias, torch.float32, "logit_bias"),
+                _p(self.sel_bias, torch.float32, "sel_bias"))
+        tail = (ctypes.cast(ys, ctypes.c_void_p), _p(self.ws, torch.uint8, "workspace"),
+                self.ws.numel(), _stream(stream))
+        if self.q8:
+            g, u, w = self.Wg.struct(), self.Wu.struct(), self.Wd.struct()
+            st = lib().moe_layer_forward_q8_host_pipelined(*head, ctypes.byref(g),
+                                                           ctypes.byref(u), ctypes.byref(w),
+                                                           *tail)
+            _check(st, "moe_layer_forward_q8_host_pipelined")
+        else:
+            st = lib().moe_layer_forward_host_pipelined(*head, _p(self.Wg, None, "Wg"),
+                                                        _p(self.Wu, None, "Wu"),
+                                                        _p(self.Wd, None, "Wd"), *tail)
+            _check(st, "moe_layer_forward_host_pipelined")
+        return y_hosts

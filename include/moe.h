@@ -366,6 +366,36 @@ moe_status moe_layer_forward_q8_host(const moe_layer_desc* desc, const void* x_h
                                      int32_t* topk_ids_out, float* topk_w_out, void* workspace,
                                      size_t ws_bytes, void* stream);
 
+/* A run of n_steps layer calls with host buffers, the copies overlapped with
+   the neighbouring steps' compute (a serving loop over batches of T tokens
+   that live in host memory, as the forward RPC delivers them).  Step i reads
+   x_host[i] ([T, d], the layer's dtype) and writes y_host[i] ([T, d] fp32);
+   its layer is exactly moe_layer_forward's (moe_layer_forward_q8's) on that
+   input, with no residual and no top-k outputs, so y_host[i] equals the
+   single call's result bit for bit.  The layer runs on `stream`; two copy
+   streams owned by the call move the data: step i + 1's input goes up while
+   step i computes, step i's output comes down while step i + 1 computes (two
+   x and two y stages in the workspace).  Ordering: the run starts after the
+   work enqueued on `stream` before the call, and `stream` waits for the last
+   copy, so work enqueued on it after the call sees every y_host[i] written.
+   Host buffers should be page-locked (otherwise the copies serialize with
+   the host).  x_host and y_host are host arrays of n_steps pointers; an entry
+   may repeat (the copies of one direction run in step order).  n_steps == 0
+   or T == 0: MOE_OK, nothing enqueued.  Errors as moe_layer_forward;
+   MOE_ERR_INVALID_ARG for n_steps < 0 or a NULL array or entry. */
+moe_status moe_layer_forward_host_pipelined(const moe_layer_desc* desc, int n_steps,
+                                            const void* const* x_host, const void* Wr,
+                                            const float* logit_bias, const float* sel_bias,
+                                            const void* Wg, const void* Wu, const void* Wd,
+                                            float* const* y_host, void* workspace,
+                                            size_t ws_bytes, void* stream);
+moe_status moe_layer_forward_q8_host_pipelined(const moe_layer_desc* desc, int n_steps,
+                                               const void* const* x_host, const void* Wr,
+                                               const float* logit_bias, const float* sel_bias,
+                                               const moe_q8_weight* Wg, const moe_q8_weight* Wu,
+                                               const moe_q8_weight* Wd, float* const* y_host,
+                                               void* workspace, size_t ws_bytes, void* stream);
+
 /* Synchronizes `stream`, then reports the sticky device flag held in the
    workspace: MOE_OK, MOE_ERR_DEVICE_INPUT or MOE_ERR_TIMEOUT (MOE_ERR_CUDA if
    the copy itself fails).  clear != 0 resets the flag afterwards.          */

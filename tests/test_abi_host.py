@@ -134,3 +134,26 @@ def test_status_strings(L):
     for s in range(7):
         assert moe.moe_status_string(s).startswith("MOE_")
     assert "unknown" in moe.moe_status_string(42)
+
+
+def test_pipelined_host_call_argument_checks(L):
+    d = _desc()
+    _, n = _ws_size(L, d)
+    two = (ctypes.c_void_p * 2)(FAKE.value, FAKE.value)
+    holed = (ctypes.c_void_p * 2)(FAKE.value, None)
+    as_vp = lambda a: ctypes.cast(a, ctypes.c_void_p)
+    for fn in (L.moe_layer_forward_host_pipelined, L.moe_layer_forward_q8_host_pipelined):
+        q8 = fn is L.moe_layer_forward_q8_host_pipelined
+        dd = _desc(dtype=moe.MOE_BF16) if q8 else d
+        _, nn = _ws_size(L, dd)
+        w = None  # weights are not reached: argument checks fail first
+        call = lambda steps, xs, ys, ws_bytes: fn(ctypes.byref(dd), steps, xs, FAKE, None, None,
+                                                  w, w, w, ys, FAKE, ws_bytes, None)
+        # no steps (or no tokens): nothing is enqueued, no device is needed
+        assert call(0, None, None, nn) == moe.MOE_OK
+        assert call(-1, as_vp(two), as_vp(two), nn) == moe.MOE_ERR_INVALID_ARG
+        assert call(2, None, as_vp(two), nn) == moe.MOE_ERR_INVALID_ARG
+        assert call(2, as_vp(two), None, nn) == moe.MOE_ERR_INVALID_ARG
+        assert call(2, as_vp(holed), as_vp(two), nn) == moe.MOE_ERR_INVALID_ARG
+        assert call(2, as_vp(two), as_vp(holed), nn) == moe.MOE_ERR_INVALID_ARG
+        assert call(2, as_vp(two), as_vp(two), nn - 256) == moe.MOE_ERR_WORKSPACE

@@ -309,6 +309,40 @@ def test_layer_forward_host_buffers(cfg):
     assert torch.equal(y_host, host(y_dev))
 
 
+# The pipelined call with host buffers: every step equals the device call on
+# its input bit for bit.  Step 0's input reaches its host buffer through a copy
+# enqueued on the stream just before the call, behind a device sleep, so an
+# upload that did not wait for the stream would read NaNs; the last output is
+# read back by a copy enqueued after the call.
+def _step_inputs(x, n):
+    return [torch.roll(x, shifts=3 * i, dims=0) * (1.0 - 0.25 * (i % 3)) for i in range(n)]
+
+
+@pytest.mark.parametrize("n_steps", [1, 2, 5])
+@pytest.mark.parametrize("cfg", [FFN_CASES[0], FFN_CASES[6]], ids=lambda c: c.name)
+def test_layer_forward_host_pipelined(cfg, n_steps):
+    inp = _case(cfg, seed=23)
+    desc = moe.desc_from_config(cfg)
+    layer = moe.MoeLayer(desc, inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"],
+                         logit_bias=inp["logit_bias"], sel_bias=inp["sel_bias"])
+    xs = _step_inputs(inp["x"], n_steps)
+    want = [host(layer.forward(x)) for x in xs]
+    torch.cuda.synchronize()
+    x_hosts = [host(x).pin_memory() for x in xs]
+    x_hosts[0].fill_(float("nan"))
+    y_hosts = [torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.float32).pin_memory()
+               for _ in range(n_steps)]
+    torch.cuda._sleep(2_000_000)  # ~1 ms of device time ahead of the copy below
+    x_hosts[0].copy_(xs[0], non_blocking=True)
+    layer.forward_host_pipelined(x_hosts, y_hosts)
+    y_last = y_hosts[-1].to(DEV, non_blocking=True)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
+    for i in range(n_steps):
+        assert torch.equal(y_hosts[i], want[i]), i
+    assert torch.equal(host(y_last), want[-1])
+
+
 # ---------------------------------------------------------------- whole layer, small
 # the largest shape the layer record admits: E=1024 routed + 4 shared experts
 # (1028 groups, the grouped GEMM's limit), top-32; softmax scores, whose gaps

@@ -168,3 +168,23 @@ def test_layer_forward_q8_host_buffers():
     torch.cuda.synchronize()
     assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
     assert torch.equal(y_host, host(y_dev))
+
+
+def test_layer_forward_q8_host_pipelined():
+    cfg = Q8_CASES[0]
+    inp = enforce_margins(make_inputs(cfg, seed=37, device=DEV), cfg, 37)
+    desc = moe.desc_from_config(cfg)
+    Wg, Wu, Wd = (moe.quantize_q8_0(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    layer = moe.MoeLayer(desc, inp["Wr"], Wg, Wu, Wd, logit_bias=inp["logit_bias"],
+                         sel_bias=inp["sel_bias"])
+    xa, xb = inp["x"], torch.roll(inp["x"], shifts=5, dims=0)
+    want = [host(layer.forward(x)) for x in (xa, xb, xa)]
+    xa_host, xb_host = host(xa).pin_memory(), host(xb).pin_memory()
+    x_hosts = [xa_host, xb_host, xa_host]  # an input buffer may repeat
+    y_hosts = [torch.full((cfg.T, cfg.d), float("nan"), dtype=torch.float32).pin_memory()
+               for _ in range(3)]
+    layer.forward_host_pipelined(x_hosts, y_hosts)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
+    for i in range(3):
+        assert torch.equal(y_hosts[i], want[i]), i
