@@ -18,6 +18,7 @@ import argparse
 import dataclasses
 import hashlib
 import json
+import re
 import math
 import os
 import statistics
@@ -165,15 +166,24 @@ def kernel_bytes(cfg, kernel, n_active_all):
     return None
 
 
+def _code_only(src):
+    """C/C++/CUDA source without comments, whitespace runs collapsed (the
+    sources carry no comment markers inside string literals)."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_source_sha(kernel):
-    """Hash of the CUDA sources a grouped-GEMM kernel is built from."""
+    """Hash of the code (comments excluded) of the CUDA sources a grouped-GEMM
+    kernel is built from."""
     csrc = os.path.join(ROOT, "expert_dispatch_gb300", "csrc")
     files = ["common.cuh", "tc_common.cuh"] + (
         ["tc_gemm_q8.cu"] if kernel.endswith("_q8") else ["tc_gemm.cu", "tc_gemm_pair.cu"])
     h = hashlib.sha256()
     for name in files:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

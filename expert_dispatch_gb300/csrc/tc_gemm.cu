@@ -16,8 +16,10 @@
 //     to BN token rows of the expert's batch, so a batch of any size down to
 //     one token costs N = 16 columns instead of a 128-row tile; weights are
 //     streamed exactly once per (expert, 128-row block, token tile).
-//   * Work unit = (expert, 128-row weight block, token tile); the order of
-//     units is described at tc::decode_unit.
+//   * Work unit = (expert, MT-row weight block, token tile), MT = 128, or 256
+//     for the decode-sized down GEMM (two 128-row boxes per stage and two
+//     accumulators, as gate/up's two matrices); the order of units is
+//     described at tc::decode_unit.
 //   * Warp 0 lane 0 issues TMA loads (128-byte swizzle) into a STAGES-deep
 //     shared-memory ring; warp 1 lane 0 issues tcgen05.mma (bf16 x bf16 ->
 //     fp32 in TMEM) and commits each stage back to the loader; warps 2-9 read
