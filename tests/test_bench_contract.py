@@ -1,9 +1,12 @@
-"""The bench's reference arm on CPU: it times the oracle, needs no GPU, and
-prints the one JSON line of the benchmark contract (rank 0 only)."""
+"""The bench's JSON line.  The reference arm times the oracle on CPU (no GPU
+needed) and prints the contract's line on rank 0 only; the GPU arm's line
+carries the roofline, per-kernel, end-to-end, clock and CPU-baseline records."""
 import json
 import os
 import subprocess
 import sys
+
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SMALL = ["--impl", "reference", "--workload", "qwen_t512", "--T", "16", "--E", "8",
@@ -44,3 +47,27 @@ def test_reference_arm_prints_nothing_on_other_ranks():
     r = _run({"CUDA_VISIBLE_DEVICES": "", "RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+# ---------------------------------------------------------------- on a GPU
+@pytest.mark.gpu
+def test_gpu_arm_prints_the_contract_line():
+    args = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "qwen_t512", "--T",
+            "64", "--E", "16", "--steps", "5", "--warmup", "3", "--cpu-budget", "1"]
+    r = subprocess.run(args, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    d = json.loads(lines[-1])
+    assert d["unit"] == "tokens/s" and d["value"] > 0 and d["n_gpus"] == 1
+    assert d["steps"] == 5 and d["warmup"] >= 3 and d["dtype"] == "bf16"
+    rf = d["roofline"]
+    assert rf["bound"] in ("hbm", "tensor") and rf["peak"] > 0
+    assert rf["achieved"] > 0 and abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
+    assert d["gpu_launches"] > 0
+    assert d["kernels"] and all(v["launches"] > 0 for v in d["kernels"].values())
+    e2e = d["e2e"]
+    assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] == 64 * 4096 * 2
+    assert e2e["d2h_bytes_per_step"] == 64 * 4096 * 4
+    assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
