@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from expert_dispatch_gb300 import moe
-from expert_dispatch_gb300.inputs import LayerConfig
+from expert_dispatch_gb300.inputs import LayerConfig, make_inputs
 from tests.helpers import W_RTOL, host, make_case, rel_err, y_tol
 
 DEV = "cuda"
@@ -83,3 +83,52 @@ def test_layer_random_sweep(seed):
                                   _deq(inp["Wu"]), _deq(inp["Wd"]), cfg.k, cfg.gate, S=cfg.S,
                                   **kw)
     assert rel_err(host(yq).double().numpy(), yq_ref) <= 1e-2, cfg
+
+
+def _host_copy(t):
+    h = moe.host_empty(t.shape, t.dtype)
+    h.copy_(t)
+    return h
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("seed", range(24))
+def test_tier_random_sweep_equals_resident(seed):
+    """The expert tier (experts in host memory, a random number of HBM slots,
+    down to one) gives the resident layer's output and routing bit for bit."""
+    rng = np.random.default_rng(70000 + seed)
+    big = rng.random() < 0.3
+    E = int(rng.integers(4, 13)) if big else int(rng.integers(4, 49))
+    k = int(rng.integers(1, min(E, 4 if big else 8) + 1))
+    T = int(rng.integers(100, 401)) if big else int(rng.integers(1, 65))
+    S = int(rng.integers(0, 3))
+    gate = int(rng.integers(0, 2))
+    d, I = 64 * int(rng.integers(1, 5)), 64 * int(rng.integers(1, 5))
+    while (E + S) * min(d, I) < 128:
+        d, I = d + 64, I + 64
+    cfg = LayerConfig("tier_sweep_%d" % seed, T=T, d=d, E=E, I=I, k=k, S=S, gate=gate,
+                      norm_topk=gate, routed_scaling=2.5 if gate else 1.0,
+                      sel_bias_range=0.1 if gate else 0.0)
+    slots = int(rng.integers(1, E + S + 1))
+    inp = make_inputs(cfg, seed=seed, device=DEV)
+    desc = moe.desc_from_config(cfg)
+    layer = moe.MoeLayer(desc, inp["Wr"], inp["Wg"], inp["Wu"], inp["Wd"],
+                         logit_bias=inp["logit_bias"], sel_bias=inp["sel_bias"])
+    tier = moe.ExpertTier(desc, inp["Wr"], *(_host_copy(inp[n]) for n in ("Wg", "Wu", "Wd")),
+                          slots * 3 * I * d * 2, logit_bias=inp["logit_bias"],
+                          sel_bias=inp["sel_bias"])
+    try:
+        g = torch.Generator(device=DEV).manual_seed(seed)
+        for _ in range(3):
+            x = torch.randn((T, d), generator=g, device=DEV).to(torch.bfloat16)
+            ids_ref = torch.empty((T, k), dtype=torch.int32, device=DEV)
+            y_ref = layer.forward(x, topk_ids=ids_ref).clone()
+            ids = torch.empty_like(ids_ref)
+            y = tier.forward(x, topk_ids=ids)
+            assert moe.moe_get_device_status(tier.ws) == moe.MOE_OK
+            assert torch.equal(ids, ids_ref) and torch.equal(y, y_ref), (cfg, slots)
+        st = tier.stats()
+        assert st["steps"] == 3 and st["resident"] <= st["n_slots"] == min(slots, E + S)
+        assert st["bytes_loaded"] == st["misses"] * 3 * I * d * 2
+    finally:
+        tier.close()
