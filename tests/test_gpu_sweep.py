@@ -4,7 +4,8 @@ sized batches (one token, top-32 of 64 experts) to batches of several hundred
 rows per expert, which take the SM-pair and 256-row GEMM paths; up to two
 shared experts, both gate families.  Routing must match bit for bit, gate
 weights within 1e-4, outputs within the layer tolerance (Q8_0: within 1e-2 of
-the oracle on the dequantized weights).  A draw whose top-(k+1) scores cannot
+the oracle on the dequantized weights); the four layer calls made one by one
+must give the fused call's result bit for bit.  A draw whose top-(k+1) scores cannot
 be separated by the routing margin (many sigmoid scores at large k) is skipped."""
 import numpy as np
 import pytest
@@ -72,6 +73,24 @@ def test_layer_random_sweep(seed):
                                  host(inp["Wu"]), host(inp["Wd"]), cfg.k, cfg.gate, S=cfg.S,
                                  **kw)
     assert rel_err(host(y).double().numpy(), y_ref) <= y_tol(cfg), cfg
+    # the four layer calls one by one give the fused call's routing and output
+    # bit for bit (the FFN call gathers rows by token_indices where the fused
+    # call scatters them by slot_row; both leave the gate weights to the combine)
+    P, i32 = cfg.T * (cfg.k + cfg.S), torch.int32
+    ws2 = moe.alloc_workspace(desc)
+    ids2, w2 = torch.empty_like(ids), torch.empty_like(w)
+    moe.moe_route(desc, inp["x"], inp["Wr"], inp["logit_bias"], inp["sel_bias"], ids2, w2, ws2)
+    off = torch.empty((cfg.E + cfg.S + 1,), dtype=i32, device=DEV)
+    tok = torch.empty((P,), dtype=i32, device=DEV)
+    sr = torch.empty((cfg.T, cfg.k + cfg.S), dtype=i32, device=DEV)
+    moe.moe_plan_dispatch(desc, ids2, None, off, tok, sr, None, None, None, ws2)
+    y_perm = torch.empty((P, cfg.d), dtype=cfg.torch_dtype, device=DEV)
+    moe.moe_expert_ffn(desc, inp["x"], off, tok, None, inp["Wg"], inp["Wu"], inp["Wd"], y_perm,
+                       ws2)
+    y2 = torch.empty_like(y)
+    moe.moe_combine(desc, y_perm, sr, w2, None, y2)
+    assert moe.moe_get_device_status(ws2) == moe.MOE_OK
+    assert torch.equal(ids2, ids) and torch.equal(w2, w) and torch.equal(y2, y), cfg
     if cfg.dtype != "bf16":
         return
     Wq = [moe.quantize_q8_0(inp[n]) for n in ("Wg", "Wu", "Wd")]
@@ -132,3 +151,54 @@ def test_tier_random_sweep_equals_resident(seed):
         assert st["bytes_loaded"] == st["misses"] * 3 * I * d * 2
     finally:
         tier.close()
+
+
+def _skewed_ids(T, E, k, rng):
+    """Distinct expert ids per token: the top k of Gumbel-perturbed Zipf(s)
+    log-weights (s = 0 is uniform), so some experts get large batches and
+    others none."""
+    s = float(rng.choice([0.0, 0.8, 1.5]))
+    logw = -s * np.log(np.arange(1, E + 1, dtype=np.float64))
+    keys = logw[None, :] + rng.gumbel(size=(T, E))
+    ids = np.argpartition(-keys, k - 1, axis=1)[:, :k]
+    order = np.argsort(-np.take_along_axis(keys, ids, 1), axis=1)  # descending score
+    return np.take_along_axis(ids, order, 1).astype(np.int32)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("seed", range(40))
+def test_plan_random_sweep(seed):
+    """moe_plan_dispatch against the oracle's plan, bit for bit, over random
+    sizes: the one-block plan and the three-kernel plan (large T x E)."""
+    rng = np.random.default_rng(90000 + seed)
+    E = int(np.exp(rng.uniform(0, np.log(1024))))
+    k = int(rng.integers(1, min(E, 32) + 1))
+    S = int(rng.integers(0, 5))
+    T = int(np.exp(rng.uniform(0, np.log(20000))))
+    T = max(1, min(T, 4_000_000 // E))
+    ids = _skewed_ids(T, E, k, rng)
+    w = rng.uniform(0, 1, (T, k)).astype(np.float32)
+    # the plan does not depend on the layer's dtype; an fp32 record admits E + S = 1
+    desc = moe.make_desc(T, 64, E, k, 64, S, dtype=moe.MOE_F32)
+    ws = moe.alloc_workspace(desc)
+    P = T * (k + S)
+    off = torch.full((E + S + 1,), -1, dtype=torch.int32, device=DEV)
+    tok = torch.full((P,), -1, dtype=torch.int32, device=DEV)
+    sr = torch.full((T, k + S), -1, dtype=torch.int32, device=DEV)
+    act = torch.full((E + S,), -1, dtype=torch.int32, device=DEV)
+    na = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    sw = torch.zeros((P,), dtype=torch.float32, device=DEV)
+    moe.moe_plan_dispatch(desc, torch.from_numpy(ids).to(DEV), torch.from_numpy(w).to(DEV), off,
+                          tok, sr, act, na, sw, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    ref = oracle.plan(ids, E, S)
+    np.testing.assert_array_equal(host(off).numpy(), ref["expert_offsets"])
+    np.testing.assert_array_equal(host(tok).numpy(), ref["token_indices"])
+    np.testing.assert_array_equal(host(sr).numpy(), ref["slot_row"])
+    n = int(host(na)[0])
+    assert n == ref["n_active"]
+    np.testing.assert_array_equal(host(act).numpy()[:n], ref["active_ids"])
+    wfull = np.concatenate([w, np.ones((T, S), np.float32)], 1)
+    exp = np.empty(P, np.float32)
+    exp[ref["slot_row"].ravel()] = wfull.ravel()
+    np.testing.assert_array_equal(host(sw).numpy(), exp)
