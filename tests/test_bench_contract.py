@@ -71,3 +71,39 @@ def test_gpu_arm_prints_the_contract_line():
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
+
+
+# ---------------------------------------------------------------- roofline logic (CPU)
+def _bench():
+    sys.path.insert(0, ROOT)
+    import bench
+    return bench
+
+
+def test_roofline_bound_follows_the_kernels_bytes_and_flops():
+    bench = _bench()
+    pk = {"hbm_gbs": 6790.7, "bf16_tflops": 1939.5, "bf16_tflops_sustained": 1708.6}
+    # default workload: 6.49 GB against 0.1 TFLOP of gate/up -> bound by HBM
+    cfg = bench.workload("qwen_t512", None, None)
+    r = bench.kernel_roofline(cfg, "ffn_gateup_tc", cfg.E, 0.95, pk, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == pk["hbm_gbs"]
+    assert abs(r["achieved"] - r["algorithmic_bytes_per_launch"] / 0.95e-3 / 1e9) < 1e-6
+    # skewed prefill: 3.3 TFLOP against 7.9 GB -> bound by the (sustained) tensor peak
+    cfg = bench.workload("skewed_zipf", None, None)
+    r = bench.kernel_roofline(cfg, "ffn_gateup_tc", cfg.E, 2.26, pk, "measured")
+    P = cfg.T * (cfg.k + cfg.S)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["peak"] == pk["bf16_tflops_sustained"]
+    assert r["algorithmic_flops_per_launch"] == 4.0 * cfg.d * cfg.I * P
+    assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
+    # the down GEMM does half the flops of gate/up per row
+    assert bench.kernel_flops(cfg, "ffn_down_tc") * 2 == bench.kernel_flops(cfg, "ffn_gateup_tc")
+
+
+def test_source_hash_ignores_comments_only():
+    bench = _bench()
+    a = "int f(int x) {  // doubles\n  return 2 * x; /* result */ }\n"
+    b = "int f(int x) {\n  /* a longer\n     note */ return 2 * x;   }"
+    c = "int f(int x) { return 3 * x; }"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
