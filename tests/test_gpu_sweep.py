@@ -202,3 +202,45 @@ def test_plan_random_sweep(seed):
     exp = np.empty(P, np.float32)
     exp[ref["slot_row"].ravel()] = wfull.ravel()
     np.testing.assert_array_equal(host(sw).numpy(), exp)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("seed", range(30))
+def test_combine_partial_random_sweep(seed):
+    """moe_combine_partial against the oracle over random sizes and random
+    availability (from every expert available to none); with every expert
+    available it equals moe_combine bit for bit."""
+    rng = np.random.default_rng(110000 + seed)
+    f32 = rng.random() < 0.3
+    E = int(rng.integers(2, 65))
+    k = int(rng.integers(1, min(E, 16) + 1))
+    S = int(rng.integers(0, 3))
+    T = int(rng.integers(1, 301))
+    d = 8 * int(rng.integers(1, 65)) if f32 else 64 * int(rng.integers(1, 9))
+    desc = moe.make_desc(T, d, E, k, 128, S, dtype=moe.MOE_F32 if f32 else moe.MOE_BF16)
+    dt = torch.float32 if f32 else torch.bfloat16
+    ids = _skewed_ids(T, E, k, rng)
+    w = rng.uniform(0.05, 1.0, (T, k)).astype(np.float32)
+    plan = oracle.plan(ids, E, S)
+    P = T * (k + S)
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    y_perm = torch.randn((P, d), generator=g, device=DEV).to(dt)
+    sr = torch.from_numpy(plan["slot_row"]).to(DEV)
+    g_ids, g_w = torch.from_numpy(ids).to(DEV), torch.from_numpy(w).to(DEV)
+    y = torch.empty((T, d), dtype=torch.float32, device=DEV)
+    miss = torch.full((T, k + S), 7, dtype=torch.int32, device=DEV)
+    everyone = torch.ones((E + S,), dtype=torch.int32, device=DEV)
+    moe.moe_combine_partial(desc, y_perm, sr, g_ids, g_w, everyone, None, y, miss)
+    y_full = torch.empty_like(y)
+    moe.moe_combine(desc, y_perm, sr, g_w, None, y_full)
+    assert torch.equal(y, y_full) and int(miss.sum()) == 0
+    p_avail = float(rng.choice([0.0, 0.3, 0.7, 1.0]))
+    avail = (rng.random(E + S) < p_avail).astype(np.int32)
+    res = torch.randn((T, d), generator=g, device=DEV) if rng.random() < 0.5 else None
+    moe.moe_combine_partial(desc, y_perm, sr, g_ids, g_w, torch.from_numpy(avail).to(DEV), res,
+                            y, miss)
+    y_ref, miss_ref = oracle.combine_partial(host(y_perm).double().numpy(), plan["slot_row"], ids,
+                                             w, avail, k, S, E, residual=host(res))
+    np.testing.assert_array_equal(host(miss).numpy(), miss_ref)
+    scale = max(float(np.abs(y_ref).max()), 1e-30)
+    assert float(np.abs(host(y).double().numpy() - y_ref).max()) / scale <= 1e-6
