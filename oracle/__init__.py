@@ -14,6 +14,10 @@ Functions (each follows the passage cited in ``oracle.c``):
   forward_sharded  the same layer grouped by expert (the workers' regrouping)
   expert_rows    one expert's SwiGLU FFN over a list of token rows
   combine        gate-weighted sum of batch rows per token plus shared rows
+  combine_partial  the combine with unavailable experts (allow_partial)
+  missing_pairs  the unserved (expert, token) pairs of a partial combine
+  quantize_q8_0 / dequantize_q8_0  Q8_0 blocks of the expert projections
+  TierOracle     the expert tier's slot assignment, step by step
 """
 from __future__ import annotations
 
@@ -71,6 +75,10 @@ def _load():
     lib.oracle_quantize_q8_0.restype = ctypes.c_int
     lib.oracle_dequantize_q8_0.argtypes = [i32, i32, i32, vp, vp, vp]
     lib.oracle_dequantize_q8_0.restype = ctypes.c_int
+    lib.oracle_missing_pairs.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
+    lib.oracle_missing_pairs.restype = ctypes.c_int
+    lib.oracle_tier_step.argtypes = [i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
+    lib.oracle_tier_step.restype = ctypes.c_int
     for f in ("oracle_router_scores", "oracle_route", "oracle_plan", "oracle_forward",
               "oracle_forward_sharded", "oracle_max_threads", "oracle_expert_rows",
               "oracle_combine"):
@@ -342,6 +350,20 @@ def combine_partial(rows, slot_row, ids, w, avail, k, S, E, residual=None):
     return y, missing
 
 
+def missing_pairs(ids, avail, k, S, E):
+    """(expert, token) of every slot whose expert did not respond, [n, 2] int32,
+    ordered by token, then slot."""
+    lib = _load()
+    idv = np.ascontiguousarray(ids, dtype=np.int32)
+    av = np.ascontiguousarray(avail, dtype=np.int32)
+    T = idv.shape[0]
+    pairs = np.empty((max(T * (k + S), 1), 2), np.int32)
+    n = np.zeros(1, np.int32)
+    _check(lib.oracle_missing_pairs(T, k, S, E, idv.ctypes.data, av.ctypes.data,
+                                    pairs.ctypes.data, n.ctypes.data), "oracle_missing_pairs")
+    return pairs[:int(n[0])].copy()
+
+
 def quantize_q8_0(w):
     """Q8_0 codes and scales of w [n_mats, R, K] (fp32 or bf16 host tensor):
     (q int8 [n_mats, R, K], scales uint16 (f16 bits) [n_mats, K/32, R])."""
@@ -365,6 +387,45 @@ def dequantize_q8_0(q, scales):
     _check(lib.oracle_dequantize_q8_0(n, R, K, q.ctypes.data, s.ctypes.data, out.ctypes.data),
            "oracle_dequantize_q8_0")
     return out
+
+
+class TierOracle:
+    """The expert tier's residency rules (oracle_tier_step in oracle.c): a
+    bounded set of slots, least-recently-used eviction, leased slots never
+    evicted, extra passes when a step's experts do not fit."""
+
+    def __init__(self, n_slots, n_experts):
+        self.n_slots, self.n_experts = int(n_slots), int(n_experts)
+        self.holder = np.full(self.n_slots, -1, np.int32)
+        self.last_use = np.zeros(self.n_slots, np.int64)
+        self.clock = np.zeros(1, np.int64)
+        self.counters = np.zeros(4, np.int64)  # hits, misses, evictions, extra passes
+
+    def step(self, experts):
+        """(slot, load, pass, n_passes) of one step's requested experts."""
+        lib = _load()
+        req = np.ascontiguousarray(experts, dtype=np.int32)
+        n = int(req.shape[0])
+        slot = np.full(max(n, 1), -1, np.int32)
+        load = np.zeros(max(n, 1), np.int32)
+        pas = np.full(max(n, 1), -1, np.int32)
+        npass = np.zeros(1, np.int32)
+        rc = lib.oracle_tier_step(self.n_slots, self.n_experts, self.holder.ctypes.data,
+                                  self.last_use.ctypes.data, self.clock.ctypes.data,
+                                  self.counters.ctypes.data, req.ctypes.data, n,
+                                  slot.ctypes.data, load.ctypes.data, pas.ctypes.data,
+                                  npass.ctypes.data)
+        _check(rc, "oracle_tier_step")
+        return slot[:n], load[:n], pas[:n], int(npass[0])
+
+    def slot_of(self, expert):
+        hit = np.nonzero(self.holder == expert)[0]
+        return int(hit[0]) if len(hit) else -1
+
+    def stats(self):
+        h, m, ev, ex = (int(v) for v in self.counters)
+        return {"steps": int(self.clock[0]), "hits": h, "misses": m, "evictions": ev,
+                "extra_passes": ex, "resident": int((self.holder >= 0).sum())}
 
 
 def widen(a):

@@ -541,6 +541,29 @@ int oracle_combine_partial(int T, int d, int k, int S, int E, const double* rows
   return OR_OK;
 }
 
+/* The unserved (expert, token) pairs of a partial combine, as a list
+ * ("Distributed MoE", failover paragraph: the pairs that could not be served
+ * are reported under `missing`).  Reading taken: token by token, slot by slot
+ * (routed slots in the routing's order, then the shared experts E+s), every
+ * pair whose expert did not respond is listed as (expert, token).
+ * pairs[2 * i], pairs[2 * i + 1] = expert, token of the i-th pair; *n = count. */
+int oracle_missing_pairs(int T, int k, int S, int E, const int32_t* ids, const int32_t* avail,
+                         int32_t* pairs, int32_t* n) {
+  if (T < 0 || k <= 0 || S < 0 || E <= 0 || !n || (T > 0 && (!ids || !avail || !pairs)))
+    return OR_EINVAL;
+  int32_t count = 0;
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k + S; ++j) {
+      const int e = j < k ? ids[(size_t)t * k + j] : E + (j - k);
+      if (avail[e]) continue;
+      pairs[2 * (size_t)count] = e;
+      pairs[2 * (size_t)count + 1] = t;
+      count += 1;
+    }
+  *n = count;
+  return OR_OK;
+}
+
 /* -------------------------------------------------------------------------
  * Q8_0 block quantization ("Distributed MoE", quantization table: 32-element
  * blocks with one f16 scale, about 8.5 bits per weight; the prepare job
@@ -605,3 +628,101 @@ void oracle_widen(const void* src, int dt, size_t n, double* dst) {
 }
 
 int oracle_max_threads(void) { return omp_get_max_threads(); }
+
+/* -------------------------------------------------------------------------
+ * Expert tier: which of a bounded set of device slots serves each expert a
+ * step needs, and which experts must be copied in.
+ *   "Distributed MoE" (tenzro docs), expert-residency paragraph: experts live
+ *     in a byte-bounded tier with least-recently-used eviction above a colder
+ *     one, and before a forward is dispatched the experts that its routing
+ *     decision selected are read ahead into the tier;
+ *   "Module expert_store" (ferrox-core docs), design list: an entry held by a
+ *     lease is never evicted, and when what a request needs does not fit, the
+ *     request is still served (by a pass-through copy): capacity pressure
+ *     costs extra transfers, never a wrong answer or a deadlock.
+ * Readings taken: one slot holds one expert's three projections (the byte
+ * budget divided by an expert's bytes); the work of a step leases every slot
+ * it reads until that work is done; when every slot is leased by the work
+ * gathered so far, that work forms a pass that runs first, its leases end,
+ * and the remaining experts form the next pass (the pass-through copy, done
+ * in slots); the experts already resident are served first (they cost no
+ * copy), then the others in request order; an expert that is missing takes
+ * an empty slot if there is one (lowest slot number), else the slot whose
+ * expert was used least recently among those not leased (lowest slot number
+ * on equal recency); recency is the step in which a slot was last used.
+ * State (owned by the caller, updated in place): holder[n_slots] (expert in
+ * each slot, -1 = empty), last_use[n_slots], clock[1] (steps so far) and
+ * counters[4] = hits, misses, evictions, extra passes.
+ * Out, per request i: slot[i], load[i] (1 = copied in this step), pass[i];
+ * *n_passes = number of passes (0 for an empty request).  A request that
+ * names an expert twice or one outside 0..n_experts-1 is refused and leaves
+ * the state unchanged.
+ * ------------------------------------------------------------------------- */
+static int tier_choose_slot(int n_slots, const int32_t* holder, const int64_t* last_use,
+                            const unsigned char* leased) {
+  for (int s = 0; s < n_slots; ++s)
+    if (!leased[s] && holder[s] < 0) return s; /* an empty slot */
+  int victim = -1;
+  for (int s = 0; s < n_slots; ++s) {
+    if (leased[s]) continue;
+    if (victim < 0 || last_use[s] < last_use[victim]) victim = s; /* least recently used */
+  }
+  return victim; /* -1: every slot is leased */
+}
+
+int oracle_tier_step(int n_slots, int n_experts, int32_t* holder, int64_t* last_use,
+                     int64_t* clock, int64_t* counters, const int32_t* req, int n,
+                     int32_t* slot, int32_t* load, int32_t* pass, int32_t* n_passes) {
+  if (n_slots <= 0 || n_experts <= 0 || n < 0 || !holder || !last_use || !clock || !counters ||
+      !n_passes)
+    return OR_EINVAL;
+  for (int i = 0; i < n; ++i) {
+    if (req[i] < 0 || req[i] >= n_experts) return OR_EINVAL;
+    for (int j = 0; j < i; ++j)
+      if (req[j] == req[i]) return OR_EINVAL;
+  }
+  unsigned char* leased = calloc((size_t)n_slots, 1);
+  unsigned char* served = calloc((size_t)(n ? n : 1), 1);
+  if (!leased || !served) {
+    free(leased);
+    free(served);
+    return OR_ENOMEM;
+  }
+  *clock += 1;
+  /* the experts already resident: no copy, leased for the first pass */
+  for (int i = 0; i < n; ++i)
+    for (int s = 0; s < n_slots; ++s)
+      if (holder[s] == req[i]) {
+        slot[i] = s;
+        load[i] = 0;
+        pass[i] = 0;
+        leased[s] = 1;
+        last_use[s] = *clock;
+        served[i] = 1;
+        counters[0] += 1;
+      }
+  /* the others, in request order, each copied into a slot */
+  int p = 0;
+  for (int i = 0; i < n; ++i) {
+    if (served[i]) continue;
+    int s = tier_choose_slot(n_slots, holder, last_use, leased);
+    if (s < 0) { /* everything leased: the pass so far runs, its leases end */
+      p += 1;
+      counters[3] += 1;
+      memset(leased, 0, (size_t)n_slots);
+      s = tier_choose_slot(n_slots, holder, last_use, leased);
+    }
+    if (holder[s] >= 0) counters[2] += 1;
+    holder[s] = req[i];
+    last_use[s] = *clock;
+    leased[s] = 1;
+    slot[i] = s;
+    load[i] = 1;
+    pass[i] = p;
+    counters[1] += 1;
+  }
+  *n_passes = n > 0 ? p + 1 : 0;
+  free(leased);
+  free(served);
+  return OR_OK;
+}

@@ -511,7 +511,45 @@ def test_partial_combine_is_a_reduced_top_k():
         np.testing.assert_allclose(y[t, p["slot_row"][t]], ref, rtol=1e-13, atol=1e-15)
 
 
+def test_missing_pairs_hand_example():
+    """Three tokens, top-2 of four experts plus one shared expert (index 4);
+    expert 2 and the shared expert are down."""
+    ids = np.array([[0, 2], [3, 1], [2, 0]], np.int32)
+    avail = np.array([1, 1, 0, 1, 0], np.int32)
+    pairs = oracle.missing_pairs(ids, avail, k=2, S=1, E=4)
+    assert pairs.tolist() == [[2, 0], [4, 0], [4, 1], [2, 2], [4, 2]]
+    assert oracle.missing_pairs(ids, np.ones(5, np.int32), 2, 1, 4).shape == (0, 2)
+
+
+def test_missing_pairs_list_the_flagged_slots():
+    """The list is the partial combine's missing mask read in row-major order
+    (numpy argwhere), each slot mapped to its expert."""
+    rng, ids, w, p = _partial_case(seed=5, T=30)
+    avail = (rng.uniform(size=7) < 0.6).astype(np.int32)
+    _, missing = oracle.combine_partial(np.eye(30 * 4), p["slot_row"], ids, w, avail, 3, 1, 6)
+    experts = np.concatenate([ids, np.full((30, 1), 6, np.int32)], axis=1)
+    want = [[int(experts[t, j]), int(t)] for t, j in np.argwhere(missing == 1)]
+    assert oracle.missing_pairs(ids, avail, 3, 1, 6).tolist() == want
+
+
 # ---------------------------------------------------------------- Q8_0 weights
+def test_q8_0_rounds_exact_halves_away_from_zero():
+    """A block whose largest magnitude is 127 has d = 1 and 1/d = 1 exactly, so
+    each code is round(w) of the stored value itself; the halves settle the
+    rounding rule of the reading taken (round half away from zero, as GGUF's
+    encoder does), which round-half-to-even would break on 0.5, 2.5 and -0.5."""
+    import torch
+    w = torch.zeros((1, 1, 32), dtype=torch.float32)
+    vals = [127.0, 0.5, -0.5, 1.5, -1.5, 2.5, -2.5, 3.5, 126.5, -126.5, 0.25, -0.75]
+    w[0, 0, :len(vals)] = torch.tensor(vals)
+    for dt in (torch.float32, torch.bfloat16):
+        q, s = oracle.quantize_q8_0(w.to(dt))
+        assert s[0, 0, 0] == 0x3C00  # f16(1.0)
+        want = [127, 1, -1, 2, -2, 3, -3, 4, 127, -127, 0, -1]
+        assert q[0, 0, :len(vals)].tolist() == want
+        assert (q[0, 0, len(vals):] == 0).all()
+
+
 def test_q8_0_round_trip_is_exact_on_representable_blocks():
     """Blocks of the form s * q (s an f16 value, integer codes with max |q| = 127)
     quantize back to exactly those codes and that scale."""

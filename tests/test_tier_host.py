@@ -1,4 +1,5 @@
-"""The expert tier's residency logic (moe_slot_cache_*), host only.
+"""The expert tier's residency logic (moe_slot_cache_*), host only, against the
+oracle's restatement of its rules (oracle_tier_step) and hand-built traces.
 
 The policy under test ("Distributed MoE" (tenzro docs), expert-residency
 paragraph: a bounded least-recently-used tier with readahead of the experts
@@ -12,56 +13,8 @@ pins are dropped.
 import numpy as np
 import pytest
 
+import oracle
 from expert_dispatch_gb300 import moe
-
-
-class ModelCache:
-    """The policy above, written out in plain Python."""
-
-    def __init__(self, n_slots, n_experts):
-        self.S = n_slots
-        self.slot_expert = [-1] * n_slots
-        self.expert_slot = [-1] * n_experts
-        self.stamp = [0] * n_slots
-        self.clock = 0
-
-    def assign(self, experts):
-        self.clock += 1
-        n = len(experts)
-        slot, load, pas = [0] * n, [0] * n, [-1] * n
-        pinned = [False] * self.S
-        for i, e in enumerate(experts):
-            s = self.expert_slot[e]
-            if s >= 0:
-                slot[i], load[i], pas[i] = s, 0, 0
-                pinned[s] = True
-                self.stamp[s] = self.clock
-
-        def pick():
-            free = [s for s in range(self.S) if not pinned[s] and self.slot_expert[s] < 0]
-            if free:
-                return free[0]
-            cands = [s for s in range(self.S) if not pinned[s]]
-            return min(cands, key=lambda s: (self.stamp[s], s)) if cands else -1
-
-        cur = 0
-        for i, e in enumerate(experts):
-            if pas[i] >= 0:
-                continue
-            s = pick()
-            if s < 0:
-                cur += 1
-                pinned = [False] * self.S
-                s = pick()
-            old = self.slot_expert[s]
-            if old >= 0:
-                self.expert_slot[old] = -1
-            self.slot_expert[s] = e
-            self.expert_slot[e] = s
-            pinned[s] = True
-            self.stamp[s] = self.clock
-            slot[i], load[i], pas[i] = s, 1, cur
-        return slot, load, pas, (cur + 1 if n else 0)
 
 
 def test_create_rejects_bad_sizes():
@@ -131,22 +84,27 @@ def test_bad_requests_leave_the_cache_unchanged():
 
 
 @pytest.mark.parametrize("n_slots,n_experts,seed", [(1, 5, 0), (3, 8, 1), (5, 40, 2),
-                                                    (16, 64, 3), (8, 8, 4)])
-def test_matches_the_policy_model(n_slots, n_experts, seed):
+                                                    (16, 64, 3), (8, 8, 4), (64, 385, 5),
+                                                    (192, 385, 6)])
+def test_matches_the_tier_oracle(n_slots, n_experts, seed):
+    """moe_slot_cache_assign against the oracle's restatement of the tier's
+    rules (oracle_tier_step), step by step: slots, loads, passes, counters and
+    the resident set, bit for bit."""
     rng = np.random.default_rng(seed)
     c = moe.SlotCache(n_slots, n_experts)
-    m = ModelCache(n_slots, n_experts)
-    hits = misses = 0
+    o = oracle.TierOracle(n_slots, n_experts)
+    p = 1.0 / np.arange(1, n_experts + 1) ** 1.1  # skewed, so some experts recur often
     for _ in range(60):
         n = int(rng.integers(0, min(n_experts, 2 * n_slots + 3) + 1))
-        # a skewed choice, so some experts recur often
-        p = 1.0 / np.arange(1, n_experts + 1) ** 1.1
-        experts = rng.choice(n_experts, size=n, replace=False, p=p / p.sum()).tolist()
-        slot, load, pas, npass = c.assign(experts)
-        ms, ml, mp, mn = m.assign(experts)
-        assert slot.tolist() == ms and load.tolist() == ml and pas.tolist() == mp and npass == mn
-        hits += n - int(load.sum())
-        misses += int(load.sum())
-        assert [c.slot_of(e) for e in range(n_experts)] == m.expert_slot
-    st = c.stats()
-    assert (st["hits"], st["misses"]) == (hits, misses)
+        experts = rng.choice(n_experts, size=n, replace=False, p=p / p.sum())
+        if rng.integers(0, 2):
+            experts = np.sort(experts)  # the tier's forward asks in ascending expert order
+        slot, load, pas, npass = c.assign(experts.tolist())
+        os_, ol, op, on = o.step(experts)
+        assert np.array_equal(slot, os_) and np.array_equal(load, ol)
+        assert np.array_equal(pas, op) and npass == on
+        assert [c.slot_of(e) for e in range(n_experts)] == [o.slot_of(e)
+                                                            for e in range(n_experts)]
+    st, ost = c.stats(), o.stats()
+    for key in ("steps", "hits", "misses", "evictions", "extra_passes", "resident"):
+        assert st[key] == ost[key], key
