@@ -154,15 +154,27 @@ def layer_work(cfg, n_active_routed, weights="dense"):
 
 
 def kernel_bytes(cfg, kernel, n_active_all):
-    """Algorithmic bytes of one launch: the weights of every active expert it
-    streams plus the rows it must read and write once."""
+    """Algorithmic bytes of one launch of an expert-FFN GEMM: the weights of
+    every active expert it must stream once.  The token rows it reads and
+    writes (x_perm, H, y_perm) are implementation traffic of the permuted
+    layout, reported by row_bytes, not counted here (as in the layer's B)."""
+    ew = (Q8_BYTES_PER_WEIGHT if kernel.endswith("_q8")
+          else (2 if cfg.dtype == "bf16" else 4))
+    if kernel in ("ffn_gateup_tc", "ffn_gateup_simt", "ffn_gateup_tc_q8"):
+        return n_active_all * 2 * cfg.I * cfg.d * ew
+    if kernel in ("ffn_down_tc", "ffn_down_simt", "ffn_down_tc_q8"):
+        return n_active_all * cfg.d * cfg.I * ew
+    return None
+
+
+def row_bytes(cfg, kernel):
+    """Bytes of the permuted token rows one GEMM launch reads and writes once."""
     P = cfg.T * (cfg.k + cfg.S)
     es = 2 if cfg.dtype == "bf16" else 4
-    ew = Q8_BYTES_PER_WEIGHT if kernel.endswith("_q8") else es
     if kernel in ("ffn_gateup_tc", "ffn_gateup_simt", "ffn_gateup_tc_q8"):
-        return n_active_all * 2 * cfg.I * cfg.d * ew + P * cfg.d * es + P * cfg.I * es
+        return P * cfg.d * es + P * cfg.I * es
     if kernel in ("ffn_down_tc", "ffn_down_simt", "ffn_down_tc_q8"):
-        return n_active_all * cfg.d * cfg.I * ew + P * cfg.I * es + P * cfg.d * es
+        return P * cfg.I * es + P * cfg.d * es
     return None
 
 
@@ -185,8 +197,12 @@ def kernel_roofline(cfg, kernel, n_active_all, ms_per_launch, pk, src):
     flops = kernel_flops(cfg, kernel)
     t = ms_per_launch / 1e3
     tc_peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
-    rec = {"kernel": kernel, "traffic": traffic_record(kernel, cfg),
-           "algorithmic_bytes_per_launch": byts, "algorithmic_flops_per_launch": flops}
+    rows = row_bytes(cfg, kernel)
+    rec = {"kernel": kernel, "traffic": traffic_record(kernel, cfg, n_active_all),
+           "algorithmic_bytes_per_launch": byts, "algorithmic_flops_per_launch": flops,
+           "row_bytes_per_launch": rows,
+           "achieved_gbs_with_rows": (byts + rows) / t / 1e9,
+           "frac_with_rows": (byts + rows) / t / 1e9 / pk["hbm_gbs"]}
     if flops / (tc_peak * 1e12) > byts / (pk["hbm_gbs"] * 1e9):
         achieved = flops / t / 1e12
         rec.update(bound="tensor", achieved=achieved, peak=tc_peak, unit="TFLOP/s",
@@ -219,9 +235,14 @@ def kernel_source_sha(kernel):
     return h.hexdigest()[:16]
 
 
-def traffic_record(kernel, cfg):
-    """dram bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel source and this workload; else None."""
+def traffic_record(kernel, cfg, n_active_all):
+    """DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) of one
+    full-size launch, or None.  The counters are taken on a small case of the
+    same layer shape (fewer experts and tokens, the same mean rows per expert,
+    so the same kernel variant, a few GB on the device), and scaled to this
+    launch by its algorithmic bytes: weights + rows of the full launch x the
+    small case's measured / algorithmic ratio.  A record counts only if it was
+    taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -229,8 +250,9 @@ def traffic_record(kernel, cfg):
         recs = json.load(f)
     sha = kernel_source_sha(kernel)
     for r in recs:
-        if r.get("kernel") == kernel and r.get("workload") == cfg.name and r.get("source") == sha:
-            return r.get("bytes_per_launch")
+        if (r.get("kernel") == kernel and r.get("workload") == cfg.name
+                and r.get("source") == sha and "ratio" in r):
+            return r["ratio"] * (kernel_bytes(cfg, kernel, n_active_all) + row_bytes(cfg, kernel))
     return None
 
 
@@ -247,26 +269,34 @@ def aggregate_ranks(ms, e2e_ms, tokens_per_step, steps, world, device):
 
 
 # ---------------------------------------------------------------- the GPU arm
-def run_gpu(args, rank, world):
-    cfg = workload(args.workload, args.T, args.E)
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    from expert_dispatch_gb300 import build
-    if rank == 0 or not os.path.exists(moe.LIB_PATH):
-        build.build()
-    if world > 1:
-        torch.distributed.barrier()
+# The workloads one default run measures: the Qwen-layout batch (the headline
+# value), DeepSeek-layout prefill, skewed (Zipf) prefill and the Kimi-layout
+# decode sweep, each with bf16 and with Q8_0 expert weights.
+SUITE = ("qwen_t512", "deepseek_prefill", "skewed_zipf", "kimi_decode@T1", "kimi_decode@T8",
+         "kimi_decode@T32", "kimi_decode@T64")
+HEADLINE = "qwen_t512"
+
+
+def measure_workload(cfg, args, weights, rank, world, dev, cpu_budget=None):
+    """One workload on this rank's GPU: W warm-up steps, K timed steps (CUDA
+    graph replay, CUDA events on the launching stream, clocks sampled), the
+    same K steps launched directly with an event pair around every library
+    launch (per-kernel times), and K end-to-end steps through the pipelined
+    host-buffer call.  Everything it allocates is freed before it returns."""
     inp = make_inputs(cfg, seed=args.seed + rank, device=dev)
     desc = moe.desc_from_config(cfg)
     Wg, Wu, Wd = inp["Wg"], inp["Wu"], inp["Wd"]
-    if args.weights == "q8_0":  # the prepare step, once, outside any timing
+    if weights == "q8_0":  # the prepare step, once, outside any timing
         Wg, Wu, Wd = (moe.quantize_q8_0(W) for W in (Wg, Wu, Wd))
     layer = moe.MoeLayer(desc, inp["Wr"], Wg, Wu, Wd, logit_bias=inp["logit_bias"],
                          sel_bias=inp["sel_bias"])
     x = inp["x"]
     y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
     ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    # The steps run on a stream of their own, which does not wait for work on
+    # the default stream: the inputs drawn above and the workspace's initial
+    # clear must be complete before the first step reads them.
+    torch.cuda.synchronize()
     stream = torch.cuda.Stream()
 
     def step():  # one layer forward on the current stream
@@ -295,7 +325,7 @@ def run_gpu(args, rank, world):
             graph.replay()
         torch.cuda.synchronize()
 
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) if rank == 0 else None
     if sampler:
         sampler.start()
     # ---- timed region (device time, CUDA events on the launching stream)
@@ -348,7 +378,6 @@ def run_gpu(args, rank, world):
     # the compute.  Two pinned x and two pinned y buffers, used in turn.
     x_ring = [x.cpu().pin_memory() for _ in range(2)]
     y_ring = [torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory() for _ in range(2)]
-    x_host, y_host = x_ring[0], y_ring[0]
 
     def host_run(n):
         layer.forward_host_pipelined([x_ring[i % 2] for i in range(n)],
@@ -365,51 +394,121 @@ def run_gpu(args, rank, world):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1)
+    if moe.moe_get_device_status(layer.ws) != moe.MOE_OK:
+        raise RuntimeError("device status not OK after the end-to-end run")
+    m = {"ms": ms, "e2e_ms": e2e_ms, "per_kernel": per_kernel, "launches": launches,
+         "graph": graph is not None, "clocks": clocks, "n_active_routed": n_active_routed,
+         "h2d": x_ring[0].numel() * x_ring[0].element_size(),
+         "d2h": y_ring[0].numel() * y_ring[0].element_size()}
+    if cpu_budget is not None:
+        m["cpu_baseline"] = cpu_baseline(cfg, inp, budget_s=cpu_budget)
+    del graph, layer, inp, Wg, Wu, Wd, x, y, ids, x_ring, y_ring
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return m
 
-    ms, e2e_ms, tokens, value = aggregate_ranks(ms, e2e_ms, cfg.T, args.steps, world, dev)
-    if rank != 0:
-        return None
-    pk, src = peaks()
-    F, B = layer_work(cfg, n_active_routed, args.weights)
+
+def workload_record(cfg, m, weights, args, world, dev, pk, src):
+    """The per-workload part of the bench line (whole-job figures over ranks)."""
+    ms, e2e_ms, tokens, value = aggregate_ranks(m["ms"], m["e2e_ms"], cfg.T, args.steps, world,
+                                                dev)
+    F, B = layer_work(cfg, m["n_active_routed"], weights)
     step_s = ms / 1e3 / args.steps
     t_star = max(F / (pk["bf16_tflops"] * 1e12), B / (pk["hbm_gbs"] * 1e9))
+    per_kernel = m["per_kernel"]
     total_kernel_ms = sum(v["ms_per_launch"] * v["launches"] for v in per_kernel.values())
     for v in per_kernel.values():
         v["share"] = v["ms_per_launch"] * v["launches"] / total_kernel_ms if total_kernel_ms else None
-    n_active_all = n_active_routed + cfg.S
+    n_active_all = m["n_active_routed"] + cfg.S
     cands = [k for k in per_kernel if kernel_bytes(cfg, k, n_active_all)]
     dom = max(cands, key=lambda k: per_kernel[k]["ms_per_launch"] * per_kernel[k]["launches"])
     roofline = kernel_roofline(cfg, dom, n_active_all, per_kernel[dom]["ms_per_launch"], pk, src)
+    return {
+        "workload": cfg.name, "expert_weights": weights,
+        "shape": {"T": cfg.T, "d": cfg.d, "E": cfg.E, "I": cfg.I, "k": cfg.k, "shared": cfg.S,
+                  "gate": "softmax" if cfg.gate == 0 else "sigmoid+bias"},
+        "tokens_per_s": value, "ms_per_step": ms / args.steps, "tokens": tokens,
+        "roofline": roofline,
+        "layer_roofline": {"flop": F, "bytes": B, "n_active_experts": m["n_active_routed"],
+                           "t_star_ms": t_star * 1e3, "frac": t_star / step_s,
+                           "tc_frac": F / step_s / (pk["bf16_tflops"] * 1e12),
+                           "hbm_frac": B / step_s / (pk["hbm_gbs"] * 1e9),
+                           "peak_source": src},
+        "kernels": per_kernel,
+        "kernel_event_sum_ms_per_step": total_kernel_ms / args.steps,
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"],
+                "call": "moe_layer_forward%s_host_pipelined, %d steps in one call"
+                        % ("_q8" if weights == "q8_0" else "", args.steps)},
+        "gpu_launches": m["launches"],
+        "launch_mode": "cuda_graph_replay" if m["graph"] else "direct",
+        "clocks": m["clocks"],
+        "l2": "inputs larger than L2: each step streams %.2f GB of expert weights" % (B / 1e9),
+    }
+
+
+def run_gpu(args, rank, world):
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from expert_dispatch_gb300 import build
+    if rank == 0 or not os.path.exists(moe.LIB_PATH):
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    pk, src = peaks()
+    if args.workload == "all":
+        names = SUITE
+        weight_sets = ("dense", "q8_0") if args.weights == "all" else (args.weights,)
+        head_name, head_weights = HEADLINE, weight_sets[0]
+    else:
+        names = (args.workload,)
+        weight_sets = ("dense",) if args.weights == "all" else (args.weights,)
+        head_name, head_weights = args.workload, weight_sets[0]
+    want_cpu = world == 1 and not args.no_cpu_baseline
+    records = {}
+    head = None
+    for weights in weight_sets:
+        for name in names:
+            cfg = workload(name, args.T, args.E)
+            is_head = (name == head_name and weights == head_weights)
+            budget = args.cpu_budget if (is_head and want_cpu and weights == "dense") else None
+            m = measure_workload(cfg, args, weights, rank, world, dev, cpu_budget=budget)
+            rec = workload_record(cfg, m, weights, args, world, dev, pk, src)
+            key = name if weights == "dense" else name + "+q8_0"
+            records[key] = rec
+            if is_head:
+                head = (cfg, m, rec)
+    if rank != 0:
+        return None
+    cfg, m, rec = head
     out = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "metric": METRIC, "value": rec["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": rec["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.dtype, "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
         "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "I": cfg.I,
-                   "k": cfg.k, "shared": cfg.S, "expert_weights": args.weights,
+                   "k": cfg.k, "shared": cfg.S, "expert_weights": head_weights,
                    "gate": "softmax" if cfg.gate == 0 else "sigmoid+bias",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2: each step streams %.1f GB of expert weights"
-                         % (B / 1e9)},
-        "roofline": roofline,
-        "layer_roofline": {"flop": F, "bytes": B, "n_active_experts": n_active_routed,
-                           "t_star_ms": t_star * 1e3, "frac": t_star / step_s,
-                           "tc_frac": F / step_s / (pk["bf16_tflops"] * 1e12),
-                           "hbm_frac": B / step_s / (pk["hbm_gbs"] * 1e9), "peak_source": src},
-        "kernels": per_kernel,
-        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
-                "d2h_bytes_per_step": y_host.numel() * y_host.element_size(),
-                "call": "moe_layer_forward%s_host_pipelined, %d steps in one call"
-                        % ("_q8" if args.weights == "q8_0" else "", args.steps)},
-        "gpu_launches": launches,
-        "launch_mode": "cuda_graph_replay" if graph is not None else "direct",
+                   "l2": rec["l2"]},
+        "roofline": rec["roofline"],
+        "layer_roofline": rec["layer_roofline"],
+        "kernels": rec["kernels"],
+        "e2e": rec["e2e"],
+        "gpu_launches": rec["gpu_launches"],
+        "launch_mode": rec["launch_mode"],
         "kernel_timing": "event pair per launch over %d directly launched steps" % args.steps,
-        "clocks": clocks,
+        "clocks": rec["clocks"],
         "published_context": PUBLISHED_CONTEXT,
     }
-    if world == 1 and not args.no_cpu_baseline and args.weights == "dense":
-        out["cpu_baseline"] = cpu_baseline(cfg, inp, budget_s=args.cpu_budget)
+    if len(records) > 1:
+        out["workloads"] = records
+        out["workloads_note"] = ("every workload timed like the headline (same K and W), one "
+                                 "workload's weights resident at a time; the headline value is "
+                                 "the %s entry" % head_name)
+    if "cpu_baseline" in m:
+        out["cpu_baseline"] = m["cpu_baseline"]
     return out
 
 
@@ -475,6 +574,7 @@ def run_tier(args, rank, world):
     xs = [torch.randn((cfg.T, cfg.d), generator=g, device=dev).to(torch.bfloat16)
           for _ in range(args.tier_inputs)]
     y = torch.empty((cfg.T, cfg.d), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()  # the steps' own stream does not wait for the default stream
     stream = torch.cuda.Stream()
 
     def timed(fn, steps):
@@ -539,72 +639,128 @@ def run_tier(args, rank, world):
 
 
 # ---------------------------------------------------------------- the oracle (CPU)
-def _oracle_inputs(cfg, inp):
-    return {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+class OracleCase:
+    """One workload's tensors on the host for the oracle: x, the router and the
+    expert projections that a token sample needs (other experts stay None, so a
+    large layer is never copied whole)."""
 
+    def __init__(self, cfg, inp):
+        self.cfg = cfg
+        self.x = inp["x"].cpu()
+        self.Wr = inp["Wr"].cpu()
+        self.lb = None if inp["logit_bias"] is None else inp["logit_bias"].cpu()
+        self.sb = None if inp["sel_bias"] is None else inp["sel_bias"].cpu()
+        self.dev_w = {n: inp[n] for n in ("Wg", "Wu", "Wd")}
+        nE = cfg.E + cfg.S
+        self.host_w = {n: [None] * nE for n in ("Wg", "Wu", "Wd")}
 
-def oracle_time(cfg, host, n_tokens, seed=0):
-    import numpy as np
+    def sample(self, n_tokens, seed):
+        import numpy as np
+        rng = np.random.default_rng(seed)
+        return np.sort(rng.choice(self.cfg.T, size=n_tokens, replace=False)).astype(np.int32)
 
-    import oracle
-    rng = np.random.default_rng(seed)
-    toks = np.sort(rng.choice(cfg.T, size=n_tokens, replace=False)).astype(np.int32)
-    t0 = time.perf_counter()
-    oracle.forward(host["x"], host["Wr"], host["Wg"], host["Wu"], host["Wd"], cfg.k, cfg.gate,
-                   S=cfg.S, norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling,
-                   logit_bias=host["logit_bias"], sel_bias=host["sel_bias"], tokens=toks)
-    return time.perf_counter() - t0
+    def fetch(self, toks):
+        """Copy to the host the experts the sampled tokens route to (untimed)."""
+        import oracle
+        cfg = self.cfg
+        ids, _ = oracle.route(self.x[torch.from_numpy(toks).long()], self.Wr, cfg.k, cfg.gate,
+                              norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling,
+                              logit_bias=self.lb, sel_bias=self.sb)
+        need = set(ids.flatten().tolist()) | set(range(cfg.E, cfg.E + cfg.S))
+        for n in ("Wg", "Wu", "Wd"):
+            for e in need:
+                if self.host_w[n][e] is None:
+                    self.host_w[n][e] = self.dev_w[n][e].cpu()
+
+    def time(self, toks):
+        """Seconds the oracle takes for the sampled tokens' layer forward."""
+        import oracle
+        cfg = self.cfg
+        self.fetch(toks)
+        t0 = time.perf_counter()
+        oracle.forward(self.x, self.Wr, self.host_w["Wg"], self.host_w["Wu"], self.host_w["Wd"],
+                       cfg.k, cfg.gate, S=cfg.S, norm_topk=cfg.norm_topk,
+                       routed_scaling=cfg.routed_scaling, logit_bias=self.lb, sel_bias=self.sb,
+                       tokens=toks)
+        return time.perf_counter() - t0
 
 
 def cpu_baseline(cfg, inp, budget_s=10.0):
     """The oracle as it stands, on this machine's cores, over a bounded token sample."""
     import oracle
-    host = _oracle_inputs(cfg, inp)
+    case = OracleCase(cfg, inp)
     cores = oracle.max_threads()
     n0 = min(cfg.T, max(1, cores))
-    t0 = oracle_time(cfg, host, n0)
+    t0 = case.time(case.sample(n0, 0))
     n = int(min(cfg.T, max(n0, n0 * budget_s / max(t0, 1e-3))))
-    t = oracle_time(cfg, host, n, seed=1) if n > n0 else t0
+    t = case.time(case.sample(n, 1)) if n > n0 else t0
     return {"value": n / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": "%d of the workload's %d tokens through the fp64 oracle (%.1f s)"
                       % (n, cfg.T, t)}
 
 
 def run_reference(args, rank, world):
+    """The oracle on this machine's cores: the headline workload for K steps
+    (after W warm-up steps), each step a token sample sized so that the run
+    ends in a few minutes; with --workload all, each other workload once more
+    on a sample of a few seconds."""
     if rank != 0:
         return None
-    cfg = workload(args.workload, args.T, args.E)
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    inp = make_inputs(cfg, seed=args.seed, device=dev)  # the same tensors the GPU arm uses
-    host = _oracle_inputs(cfg, inp)
-    del inp
     import oracle
     oracle.build()
     cores = oracle.max_threads()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    head_name = HEADLINE if args.workload == "all" else args.workload
+    cfg = workload(head_name, args.T, args.E)
+    inp = make_inputs(cfg, seed=args.seed, device=dev)  # the same tensors the GPU arm uses
+    case = OracleCase(cfg, inp)
+    del inp
     # size one step's sample so that warm-up + steps finish in a few minutes
     n_cal = min(cfg.T, max(1, cores))
-    t_cal = oracle_time(cfg, host, n_cal)
-    per_tok = t_cal / n_cal
-    per_step_budget = min(20.0, 150.0 / max(1, args.steps + args.warmup))
+    per_tok = case.time(case.sample(n_cal, 0)) / n_cal
+    per_step_budget = min(20.0, 120.0 / max(1, args.steps + args.warmup))
     n = int(min(cfg.T, max(1, per_step_budget / per_tok)))
     for i in range(args.warmup):
-        oracle_time(cfg, host, n, seed=100 + i)
-    times = [oracle_time(cfg, host, n, seed=i) for i in range(args.steps)]
+        case.time(case.sample(n, 100 + i))
+    times = [case.time(case.sample(n, i)) for i in range(args.steps)]
     total = sum(times)
     value = n * args.steps / total
-    return {
+    del case
+    out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) activations, N(0,1/fan_in) weights)",
         "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "I": cfg.I,
-                   "k": cfg.k, "shared": cfg.S},
+                   "k": cfg.k, "shared": cfg.S, "expert_weights": "dense",
+                   "gate": "softmax" if cfg.gate == 0 else "sigmoid+bias",
+                   "parallelism": "single GPU" if world == 1 else "replicas"},
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": "%d of the workload's %d tokens per step" % (n, cfg.T)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+    if args.workload == "all":
+        recs = {}
+        for name in SUITE:
+            if name == head_name:
+                continue
+            wcfg = workload(name, args.T, args.E)
+            inp = make_inputs(wcfg, seed=args.seed, device=dev)
+            case = OracleCase(wcfg, inp)
+            del inp
+            n0 = min(wcfg.T, max(1, cores // 2))
+            t0 = case.time(case.sample(n0, 0))
+            nn = int(min(wcfg.T, max(n0, n0 * 3.0 / max(t0, 1e-3))))
+            tt = case.time(case.sample(nn, 1)) if nn > n0 else t0
+            recs[name] = {"workload": wcfg.name, "tokens_per_s": nn / tt, "cores": cores,
+                          "sample": "%d of the workload's %d tokens (%.1f s)" % (nn, wcfg.T, tt)}
+            del case
+            if dev == "cuda":
+                torch.cuda.empty_cache()
+        out["workloads"] = recs
+    return out
 
 
 def main():
@@ -612,8 +768,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="qwen_t512",
-                    help="tiny_fp32 | qwen_t512 | deepseek_prefill | skewed_zipf | "
+    ap.add_argument("--workload", default="all",
+                    help="all (every workload below but the tiny one; the headline is "
+                         "qwen_t512) | tiny_fp32 | qwen_t512 | deepseek_prefill | skewed_zipf | "
                          "kimi_decode@T{1,8,32,64}")
     ap.add_argument("--T", type=int, default=None, help="override the workload's tokens")
     ap.add_argument("--E", type=int, default=None, help="override the workload's experts")
@@ -621,8 +778,9 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--weights", default="dense", choices=("dense", "q8_0"),
-                    help="expert weights in the layer's dtype, or Q8_0 blocks")
+    ap.add_argument("--weights", default="all", choices=("all", "dense", "q8_0"),
+                    help="expert weights in the layer's dtype, Q8_0 blocks, or both (with "
+                         "--workload all; a single workload then runs dense)")
     ap.add_argument("--no-graph", dest="graph", action="store_false",
                     help="time direct launches instead of CUDA-graph replays")
     ap.add_argument("--tier-slots", type=int, default=0,

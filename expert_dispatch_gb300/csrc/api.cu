@@ -758,6 +758,19 @@ moe_status moe_combine_partial(const moe_layer_desc* desc, const void* y_perm,
                                             static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_partial_missing_pairs(const moe_layer_desc* desc, const int32_t* topk_ids,
+                                    const int32_t* missing, int32_t* pairs, int32_t* n_pairs,
+                                    void* stream) {
+  const NvtxRange nvtx("moe_partial_missing_pairs");
+  moe_status st = check_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!n_pairs) return MOE_ERR_INVALID_ARG;
+  if (desc->T > 0 && (!topk_ids || !missing || !pairs)) return MOE_ERR_INVALID_ARG;
+  if (pairs && (reinterpret_cast<uintptr_t>(pairs) & 7u)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_missing_pairs(topk_ids, missing, desc->T, desc->k, desc->S, desc->E,
+                                          pairs, n_pairs, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_layer_forward(const moe_layer_desc* desc, const void* x, const void* Wr,
                              const float* logit_bias, const float* sel_bias, const void* Wg,
                              const void* Wu, const void* Wd, const float* residual, float* y,

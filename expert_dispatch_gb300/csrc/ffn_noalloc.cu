@@ -22,8 +22,11 @@
 //     different host threads on the same device) race with each other; they
 //     must be ordered by the caller;
 //   * the first call on each device looks up the array's device address with
-//     that device current (cudaGetSymbolAddress); that first call should come
-//     before any stream capture;
+//     that device current (cudaGetSymbolAddress) and keeps it for the life of
+//     the process; that first call should come before any stream capture;
+//   * after a device reset (cudaDeviceReset) the library's device code may be
+//     reloaded at another address, so the kept address is stale: do not call
+//     this entry point on a device after resetting it;
 //   * the kernels' error word lives in the array and is cleared at every
 //     call; device-detected problems are not reported by this entry point.
 #include <cuda_runtime.h>

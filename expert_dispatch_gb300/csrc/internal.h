@@ -167,6 +167,11 @@ cudaError_t launch_combine_partial(int dtype, const void* y_perm, const int32_t*
                                    int k, int S, int E, float* y, int32_t* missing,
                                    cudaStream_t s);
 
+// (expert, token) of every slot flagged in missing [T, k+S], token-major
+cudaError_t launch_missing_pairs(const int32_t* ids, const int32_t* missing, int T, int k,
+                                 int S, int E, int32_t* pairs, int32_t* n_pairs,
+                                 cudaStream_t s);
+
 int num_sms();
 
 // Expert residency in a bounded set of device slots (slot_cache.cu).

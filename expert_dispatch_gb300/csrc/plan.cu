@@ -128,12 +128,13 @@ __global__ void plan_place(const int32_t* __restrict__ ids, const float* __restr
                            int T, int E, int k, int S, const uint32_t* __restrict__ bits, int nw,
                            const int32_t* __restrict__ wpre, const int32_t* __restrict__ offsets,
                            int32_t* __restrict__ tok_idx, int32_t* __restrict__ slot_row,
-                           float* __restrict__ slot_w) {
+                           float* __restrict__ slot_w, int* __restrict__ flags) {
   pdl_wait();     // the predecessor grid is complete and visible
   pdl_trigger();  // dependents may launch (they wait for this grid in turn)
   const long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int ks = k + S;
-  if (p >= (long long)T * ks) return;
+  const long long P = (long long)T * ks;
+  if (p >= P) return;
   const int t = (int)(p / ks), j = (int)(p % ks);
   const int e = rp::pair_expert(ids, t, j, k, E);
   if (j < k && (e < 0 || e >= E)) {
@@ -142,7 +143,12 @@ __global__ void plan_place(const int32_t* __restrict__ ids, const float* __restr
   }
   const size_t wi = (size_t)e * nw + (t >> 5);
   const uint32_t below = bits[wi] & ((1u << (t & 31)) - 1u);
-  const int pos = offsets[e] + wpre[wi] + __popc(below);
+  const long long pos = (long long)offsets[e] + wpre[wi] + __popc(below);
+  if (pos < 0 || pos >= P) {  // offsets not made by this plan's scan: flagged, not written
+    flag_error(flags, kErrDeviceInput);
+    slot_row[p] = -1;
+    return;
+  }
   tok_idx[pos] = t;
   slot_row[p] = pos;
   if (slot_w) slot_w[pos] = (j < k && topk_w) ? topk_w[(size_t)t * k + j] : 1.f;
@@ -201,8 +207,8 @@ cudaError_t launch_plan(const int32_t* ids, const float* topk_w, int T, int E, i
   }
   {
     ProfScope pr("plan_place", s);
-    (void)launch_kernel(plan_place, nb, 256, 0, s, ids, topk_w, T, E, k, S, bits, nw, wpre, offsets, tok_idx,
-                                  slot_row, slot_w);
+    (void)launch_kernel(plan_place, nb, 256, 0, s, ids, topk_w, T, E, k, S, bits, nw, wpre,
+                        offsets, tok_idx, slot_row, slot_w, flags);
   }
   return cudaGetLastError();
 }

@@ -110,10 +110,11 @@ constexpr int kScatterThreads = 256;
 constexpr int kScatterBatch = 8;      // 16-byte vectors in flight per thread
 constexpr int kScatterMaxSlots = 36;  // k <= 32, S <= 4
 
-// Block per token t: its slot rows are staged in shared memory (a dropped
-// slot, -1, is skipped; a row outside the batch rows is flagged and
-// skipped), then each thread loads up to kScatterBatch 16-byte vectors of
-// x[t] and stores them to every slot row.  TO_F16: bf16 in, fp16 out.
+// Block per token t (gridDim.x = T): its slot rows are staged in shared
+// memory (a dropped slot, -1, is skipped; a row outside the batch rows or
+// beyond the T * ks rows of x_perm is flagged and skipped), then each thread
+// loads up to kScatterBatch 16-byte vectors of x[t] and stores them to every
+// slot row.  TO_F16: bf16 in, fp16 out.
 template <bool TO_F16>
 __global__ void __launch_bounds__(kScatterThreads)
     scatter_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ slot_row,
@@ -125,7 +126,8 @@ __global__ void __launch_bounds__(kScatterThreads)
   const int t = blockIdx.x;
   if (threadIdx.x < ks) {
     const int r = slot_row[(size_t)t * ks + threadIdx.x];
-    const bool bad = r >= *total_rows || r < -1;
+    const long long cap = (long long)gridDim.x * ks;
+    const bool bad = r >= *total_rows || r < -1 || (long long)r >= cap;
     if (bad) flag_error(flags, kErrDeviceInput);
     rows_s[threadIdx.x] = bad ? -1 : r;
   }
@@ -327,6 +329,60 @@ __global__ void __launch_bounds__(128) combine_partial_kernel(
   dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
 }
 
+// The unserved (expert, token) pairs of a partial combine, as a list
+// ("Distributed MoE", failover paragraph: the pairs allow_partial could not
+// serve are reported under `missing`).  One block: thread i owns a contiguous
+// run of the T * (k + S) slots in token-major order, counts its flagged
+// slots, a block-wide exclusive scan gives each run its first output index,
+// and the run writes (expert, token) for each flagged slot in slot order.
+// The list is therefore ordered by token, then slot.  A flagged routed slot
+// whose id lies outside [0, E) is listed with that id as it stands.
+constexpr int kMissThreads = 1024;
+
+__global__ void __launch_bounds__(kMissThreads)
+    missing_pairs_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ missing,
+                         int T, int k, int S, int E, int2* __restrict__ pairs,
+                         int32_t* __restrict__ n_pairs) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int warp_sums[kMissThreads / 32];
+  const int ks = k + S;
+  const long long n = (long long)T * ks;
+  const long long per = (n + kMissThreads - 1) / kMissThreads;
+  const long long lo = min(n, per * threadIdx.x), hi = min(n, lo + per);
+  int cnt = 0;
+  for (long long i = lo; i < hi; ++i) cnt += missing[i] != 0;
+  // block-wide exclusive scan of cnt
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = warp_sums[lane];
+    int vi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, vi, o);
+      if (lane >= o) vi += u;
+    }
+    warp_sums[lane] = vi - v;
+    if (lane == 31) *n_pairs = vi;
+  }
+  __syncthreads();
+  int out = warp_sums[warp] + incl - cnt;
+  for (long long i = lo; i < hi; ++i) {
+    if (missing[i] == 0) continue;
+    const int t = (int)(i / ks), j = (int)(i % ks);
+    const int e = j < k ? ids[(size_t)t * k + j] : E + (j - k);
+    pairs[out++] = make_int2(e, t);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_combine_partial(int dtype, const void* y_perm, const int32_t* slot_row,
@@ -344,6 +400,16 @@ cudaError_t launch_combine_partial(int dtype, const void* y_perm, const int32_t*
   else
     (void)launch_kernel(combine_partial_kernel<false>, grid, 128, 0, s, y_perm, slot_row, ids,
                         topk_w, avail, residual, d, k, S, E, P, y, missing);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_missing_pairs(const int32_t* ids, const int32_t* missing, int T, int k,
+                                 int S, int E, int32_t* pairs, int32_t* n_pairs,
+                                 cudaStream_t s) {
+  if (T == 0) return cudaMemsetAsync(n_pairs, 0, sizeof(int32_t), s);
+  ProfScope pr("missing_pairs", s);
+  (void)launch_kernel(missing_pairs_kernel, 1, kMissThreads, 0, s, ids, missing, T, k, S, E,
+                      reinterpret_cast<int2*>(pairs), n_pairs);
   return cudaGetLastError();
 }
 

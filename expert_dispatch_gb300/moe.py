@@ -38,7 +38,8 @@ MOE_BF16 = 1
 EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_dispatch",
             "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status",
             "moe_status_string", "moe_launch_count", "moe_profile_enable", "moe_profile_query",
-            "moe_expert_ffn_noalloc", "moe_combine_partial", "moe_quantize_q8_0",
+            "moe_expert_ffn_noalloc", "moe_combine_partial", "moe_partial_missing_pairs",
+            "moe_quantize_q8_0",
             "moe_expert_ffn_q8", "moe_layer_forward_q8", "moe_slot_cache_create",
             "moe_slot_cache_destroy", "moe_slot_cache_assign", "moe_slot_cache_slot_of",
             "moe_slot_cache_get_stats", "moe_tier_create", "moe_tier_destroy",
@@ -119,6 +120,7 @@ def lib():
     L.moe_launch_count.restype = ctypes.c_int64
     L.moe_expert_ffn_noalloc.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.moe_combine_partial.argtypes = [D, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.moe_partial_missing_pairs.argtypes = [D, vp, vp, vp, vp, vp]
     Q = ctypes.POINTER(Q8WeightStruct)
     L.moe_quantize_q8_0.argtypes = [i32, i32, i32, i32, vp, vp, vp, vp]
     L.moe_expert_ffn_q8.argtypes = [D, vp, vp, vp, vp, Q, Q, Q, vp, vp, sz, vp]
@@ -319,6 +321,22 @@ def moe_combine_partial(desc, y_perm, slot_row, topk_ids, topk_w, expert_availab
         _p(residual, torch.float32, "residual"), _p(y, torch.float32, "y"),
         _p(missing, torch.int32, "missing"), _stream(stream))
     _check(st, "moe_combine_partial")
+
+
+def moe_partial_missing_pairs(desc, topk_ids, missing, pairs, n_pairs, stream=None):
+    """The (expert, token) pairs flagged in a partial combine's missing mask,
+    written to pairs[T*(k+S), 2] in token, then slot order; n_pairs[1] gets the
+    count."""
+    ks = desc.k + desc.S
+    _need(topk_ids, (desc.T, desc.k), "topk_ids")
+    _need(missing, (desc.T, ks), "missing")
+    _need(pairs, (desc.T * ks, 2), "pairs")
+    _need(n_pairs, (1,), "n_pairs")
+    st = lib().moe_partial_missing_pairs(
+        ctypes.byref(desc), _p(topk_ids, torch.int32, "topk_ids"),
+        _p(missing, torch.int32, "missing"), _p(pairs, torch.int32, "pairs"),
+        _p(n_pairs, torch.int32, "n_pairs"), _stream(stream))
+    _check(st, "moe_partial_missing_pairs")
 
 
 def moe_layer_forward(desc, x, Wr, logit_bias, sel_bias, Wg, Wu, Wd, residual, y, topk_ids_out,

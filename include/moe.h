@@ -168,7 +168,10 @@ moe_status moe_expert_ffn(const moe_layer_desc* desc, const void* x,
        contents: calls that overlap on the GPU race, so the caller must order
        them (one stream, or explicit dependencies);
      - the first call on each device looks up the array's address with that
-       device current; make that first call before any stream capture;
+       device current and keeps it; make that first call before any stream
+       capture; the kept address does not survive a device reset
+       (cudaDeviceReset), so the call must not be used on a device after it
+       has been reset;
      - device-detected problems (bad token indices, timeouts) are not reported
        by this call; use moe_expert_ffn with a workspace to see them.
    Nothing is allocated: no cudaMalloc, cudaFree or allocating library call. */
@@ -209,6 +212,22 @@ moe_status moe_combine_partial(const moe_layer_desc* desc, const void* y_perm,
                                const float* topk_w, const int32_t* expert_available,
                                const float* residual, float* y, int32_t* missing,
                                void* stream);
+
+/* moe_partial_missing_pairs -- the unserved pairs of a partial combine as a
+   list ("Distributed MoE", failover paragraph: allow_partial reports the
+   (expert, token) pairs it could not serve under `missing`).
+     topk_ids [T, k] int32: the routing given to moe_combine_partial.
+     missing  [T, k+S] int32: the mask moe_combine_partial wrote.
+     pairs    [T*(k+S), 2] int32 out (8-byte aligned): (expert, token) of
+              every flagged slot, ordered by token, then slot (the shared
+              expert s of a token is expert E+s); entries past the count are
+              left untouched.
+     n_pairs  [1] int32 out: the number of pairs.
+   Device pointers, caller-owned; stream-ordered.  T == 0 writes a count of
+   0.  Argument errors return before any launch. */
+moe_status moe_partial_missing_pairs(const moe_layer_desc* desc, const int32_t* topk_ids,
+                                     const int32_t* missing, int32_t* pairs, int32_t* n_pairs,
+                                     void* stream);
 
 /* moe_layer_forward -- gate -> plan -> expert FFN -> combine ("Distributed
    MoE", RPC list: forward).  topk_ids_out [T, k] / topk_w_out [T, k] may be

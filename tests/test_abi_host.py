@@ -157,3 +157,16 @@ def test_pipelined_host_call_argument_checks(L):
         assert call(2, as_vp(holed), as_vp(two), nn) == moe.MOE_ERR_INVALID_ARG
         assert call(2, as_vp(two), as_vp(holed), nn) == moe.MOE_ERR_INVALID_ARG
         assert call(2, as_vp(two), as_vp(two), nn - 256) == moe.MOE_ERR_WORKSPACE
+
+
+def test_missing_pairs_argument_checks(L):
+    d = _desc()
+    fn = L.moe_partial_missing_pairs
+    assert fn(ctypes.byref(d), FAKE, FAKE, FAKE, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert fn(ctypes.byref(d), None, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG
+    assert fn(ctypes.byref(d), FAKE, None, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG
+    assert fn(ctypes.byref(d), FAKE, FAKE, None, FAKE, None) == moe.MOE_ERR_INVALID_ARG
+    assert fn(ctypes.byref(d), FAKE, FAKE, ctypes.c_void_p(0x10004), FAKE, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    bad = _desc(k=0)
+    assert fn(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, None) == moe.MOE_ERR_INVALID_ARG

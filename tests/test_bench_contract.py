@@ -73,6 +73,28 @@ def test_gpu_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cores"] >= 1
 
 
+@pytest.mark.gpu
+def test_gpu_arm_runs_every_workload_in_one_line():
+    """The default run: every workload, bf16 and Q8_0 experts, one after another
+    in one process (small shapes here), the headline being the Qwen-layout one."""
+    args = [sys.executable, os.path.join(ROOT, "bench.py"), "--T", "64", "--E", "16", "--steps",
+            "4", "--warmup", "3", "--no-cpu-baseline"]
+    r = subprocess.run(args, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    d = json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
+    sys.path.insert(0, ROOT)
+    import bench
+    w = d["workloads"]
+    assert set(w) == set(bench.SUITE) | {n + "+q8_0" for n in bench.SUITE}
+    assert d["value"] == w[bench.HEADLINE]["tokens_per_s"]
+    for name, rec in w.items():
+        assert rec["tokens_per_s"] > 0 and rec["ms_per_step"] > 0, name
+        assert rec["expert_weights"] == ("q8_0" if name.endswith("+q8_0") else "dense")
+        assert rec["roofline"]["frac"] > 0 and rec["layer_roofline"]["t_star_ms"] > 0
+        assert rec["e2e"]["value"] > 0 and rec["gpu_launches"] > 0
+        assert "sm_mhz" in rec["clocks"]
+
+
 # ---------------------------------------------------------------- roofline logic (CPU)
 def _bench():
     sys.path.insert(0, ROOT)

@@ -3,7 +3,8 @@
 Routing (ids) and the dispatch plan must match bit-exactly; gate weights within
 the fp32-accumulation bound; layer outputs within max|dy|/max|y| <= 1e-5 (fp32
 layer) or 1e-2 (bf16 layer).  Small cases span several tiles and ragged tails;
-the five workloads run at full size with sampled tokens checked one by one.
+the five workloads run at full size with every token checked against the
+per-token oracle.
 """
 import numpy as np
 import pytest
@@ -13,7 +14,8 @@ import oracle
 from expert_dispatch_gb300 import moe
 from expert_dispatch_gb300.inputs import (CONFIGS, DECODE_TS, KIMI_DECODE, LayerConfig,
                                           make_inputs)
-from tests.helpers import W_RTOL, enforce_margins, host, rel_err, y_tol
+from tests.helpers import (check_all_tokens, check_weights, enforce_margins, host, rel_err,
+                           y_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -96,7 +98,7 @@ def test_route_parity(cfg):
     ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
                                   **_oracle_kw(cfg, inp))
     np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
-    np.testing.assert_allclose(host(w).numpy(), w_ref, rtol=W_RTOL, atol=0)
+    check_weights(host(w).numpy(), w_ref, inp, cfg)
 
 
 # ---------------------------------------------------------------- planner
@@ -361,7 +363,7 @@ def test_layer_forward_parity_small(cfg):
     ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
                                   **_oracle_kw(cfg, inp))
     np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
-    np.testing.assert_allclose(host(w).numpy(), w_ref, rtol=W_RTOL, atol=0)
+    check_weights(host(w).numpy(), w_ref, inp, cfg)
     y_ref, _, _ = _oracle_forward(cfg, inp, np.arange(cfg.T, dtype=np.int32), ids_ref,
                                   residual=residual)
     # the residual is exact in fp32; compare the MoE part against its own scale
@@ -399,7 +401,7 @@ def test_layer_forward_random_tiny_shapes(seed):
     ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
                                   **_oracle_kw(cfg, inp))
     np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
-    np.testing.assert_allclose(host(w).numpy(), w_ref, rtol=W_RTOL, atol=0)
+    check_weights(host(w).numpy(), w_ref, inp, cfg)
     y_ref, _, _ = _oracle_forward(cfg, inp, np.arange(cfg.T, dtype=np.int32), ids_ref)
     assert rel_err(host(y).double().numpy(), y_ref) <= y_tol(cfg), (cfg, rel_err(host(y).double().numpy(), y_ref))
 
@@ -426,13 +428,15 @@ def test_layer_forward_is_deterministic():
 
 
 # ---------------------------------------------------------------- the five workloads, full size
-def _full_size(cfg, n_sample, seed=0):
+def _full_size(cfg, seed=0):
+    """The workload at full size: routing and plan bit-exact on all tokens, and
+    every token's output against the per-token oracle."""
     inp = _case(cfg, seed=seed)
     y, ids, w, ws = _gpu_layer(cfg, inp)
     ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
                                   **_oracle_kw(cfg, inp))
     np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
-    np.testing.assert_allclose(host(w).numpy(), w_ref, rtol=W_RTOL, atol=0)
+    check_weights(host(w).numpy(), w_ref, inp, cfg)
     # the plan of the full routing, bit-exact
     desc = moe.desc_from_config(cfg)
     P = cfg.T * (cfg.k + cfg.S)
@@ -444,38 +448,36 @@ def _full_size(cfg, n_sample, seed=0):
     np.testing.assert_array_equal(host(off).numpy(), ref["expert_offsets"])
     np.testing.assert_array_equal(host(tok).numpy(), ref["token_indices"])
     np.testing.assert_array_equal(host(sr).numpy(), ref["slot_row"])
-    # sampled tokens through the oracle, one by one
-    rng = np.random.default_rng(seed)
-    n = min(n_sample, cfg.T)
-    tokens = np.sort(rng.choice(cfg.T, size=n, replace=False)).astype(np.int32)
-    y_ref, _, _ = _oracle_forward(cfg, inp, tokens, ids_ref)
-    got = host(y[torch.from_numpy(tokens).long().to(DEV)]).double().numpy()
-    assert np.isfinite(host(y).numpy()).all()
-    err = rel_err(got, y_ref)
-    assert err <= y_tol(cfg), err
-    del inp, y, ws
+    y_host = host(y).double().numpy()
+    del y, ws
+    torch.cuda.empty_cache()
+    # every token through the oracle, one by one
+    y_ref, ids_o, _ = _oracle_forward(cfg, inp, np.arange(cfg.T, dtype=np.int32), ids_ref)
+    np.testing.assert_array_equal(ids_o, ids_ref)
+    check_all_tokens(y_host, y_ref, ids_ref, cfg, y_tol(cfg))
+    del inp
     torch.cuda.empty_cache()
 
 
 def test_full_tiny_fp32():
-    _full_size(CONFIGS["tiny_fp32"], n_sample=64)
+    _full_size(CONFIGS["tiny_fp32"])
 
 
 def test_full_qwen_t512():
-    _full_size(CONFIGS["qwen_t512"], n_sample=48)
+    _full_size(CONFIGS["qwen_t512"])
 
 
 def test_full_deepseek_prefill():
-    _full_size(CONFIGS["deepseek_prefill"], n_sample=8)
+    _full_size(CONFIGS["deepseek_prefill"])
 
 
 def test_full_skewed_zipf():
-    _full_size(CONFIGS["skewed_zipf"], n_sample=24)
+    _full_size(CONFIGS["skewed_zipf"])
 
 
 @pytest.mark.parametrize("T", DECODE_TS)
 def test_full_kimi_decode(T):
-    _full_size(KIMI_DECODE.with_T(T), n_sample=8)
+    _full_size(KIMI_DECODE.with_T(T))
 
 
 # ---------------------------------------------------------------- partial combine
@@ -516,3 +518,12 @@ def test_combine_partial_parity(cfg):
                                              cfg.S, cfg.E, residual=host(res))
     np.testing.assert_array_equal(host(miss).numpy(), miss_ref)
     assert rel_err(host(y).numpy(), y_ref) <= 1e-6
+    # the unserved (expert, token) pairs as a list
+    pairs = torch.full((P, 2), -9, dtype=torch.int32, device=DEV)
+    n_pairs = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    moe.moe_partial_missing_pairs(desc, g_ids, miss, pairs, n_pairs)
+    want = oracle.missing_pairs(ids, avail, cfg.k, cfg.S, cfg.E)
+    n = int(host(n_pairs)[0])
+    assert n == len(want) > 0
+    np.testing.assert_array_equal(host(pairs).numpy()[:n], want)
+    assert bool((pairs[n:] == -9).all())

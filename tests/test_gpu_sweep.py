@@ -14,7 +14,7 @@ import torch
 import oracle
 from expert_dispatch_gb300 import moe
 from expert_dispatch_gb300.inputs import LayerConfig, make_inputs
-from tests.helpers import W_RTOL, host, make_case, rel_err, y_tol
+from tests.helpers import check_weights, host, make_case, rel_err, y_tol
 
 DEV = "cuda"
 
@@ -68,7 +68,7 @@ def test_layer_random_sweep(seed):
     assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
     ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate, **kw)
     np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
-    np.testing.assert_allclose(host(w).numpy(), w_ref, rtol=W_RTOL, atol=0)
+    check_weights(host(w).numpy(), w_ref, inp, cfg)
     y_ref, _, _ = oracle.forward(host(inp["x"]), host(inp["Wr"]), host(inp["Wg"]),
                                  host(inp["Wu"]), host(inp["Wd"]), cfg.k, cfg.gate, S=cfg.S,
                                  **kw)
@@ -209,7 +209,8 @@ def test_plan_random_sweep(seed):
 def test_combine_partial_random_sweep(seed):
     """moe_combine_partial against the oracle over random sizes and random
     availability (from every expert available to none); with every expert
-    available it equals moe_combine bit for bit."""
+    available it equals moe_combine bit for bit; the list of unserved pairs
+    (moe_partial_missing_pairs) equals the oracle's."""
     rng = np.random.default_rng(110000 + seed)
     f32 = rng.random() < 0.3
     E = int(rng.integers(2, 65))
@@ -244,3 +245,10 @@ def test_combine_partial_random_sweep(seed):
     np.testing.assert_array_equal(host(miss).numpy(), miss_ref)
     scale = max(float(np.abs(y_ref).max()), 1e-30)
     assert float(np.abs(host(y).double().numpy() - y_ref).max()) / scale <= 1e-6
+    pairs = torch.full((P, 2), -9, dtype=torch.int32, device=DEV)
+    n_pairs = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    moe.moe_partial_missing_pairs(desc, g_ids, miss, pairs, n_pairs)
+    want = oracle.missing_pairs(ids, avail, k, S, E)
+    n = int(host(n_pairs)[0])
+    assert n == len(want)
+    np.testing.assert_array_equal(host(pairs).numpy()[:n], want)

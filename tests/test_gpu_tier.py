@@ -1,13 +1,18 @@
 """GPU: the expert tier (moe_tier_*) -- experts in host memory, a bounded pool of
 HBM slots -- gives moe_layer_forward's result bit for bit, whatever the budget
 ("Module expert_store" (ferrox-core docs): the cached path proven bit-identical
-to the resident one at generous and at smaller-than-one-step budgets)."""
+to the resident one at generous and at smaller-than-one-step budgets); its
+output matches the fp64 oracle's layer forward, and its hit / miss / eviction
+/ extra-pass counters match the oracle's restatement of the tier's rules
+(oracle_tier_step) replayed on the oracle's routing of the same steps."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from expert_dispatch_gb300 import moe
 from expert_dispatch_gb300.inputs import KIMI_DECODE, LayerConfig, make_inputs
+from tests.helpers import enforce_margins, host, rel_err, y_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -52,10 +57,39 @@ def _tier(cfg, inp, slots):
                           sel_bias=inp["sel_bias"])
 
 
-def _xs(cfg, n, seed):
+def _xs(cfg, n, seed, inp=None):
+    """n token batches; with the layer's inputs given, each batch keeps every
+    routing decision clear of near-ties (so that routing is comparable with the
+    oracle's bit for bit)."""
     g = torch.Generator(device=DEV).manual_seed(seed)
-    return [torch.randn((cfg.T, cfg.d), generator=g, device=DEV).to(torch.bfloat16)
-            for _ in range(n)]
+    xs = [torch.randn((cfg.T, cfg.d), generator=g, device=DEV).to(torch.bfloat16)
+          for _ in range(n)]
+    if inp is not None:
+        for i, x in enumerate(xs):
+            enforce_margins(dict(inp, x=x), cfg, seed * 100 + i)
+    return xs
+
+
+def _oracle_kw(cfg, inp):
+    return dict(norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling,
+                logit_bias=host(inp["logit_bias"]), sel_bias=host(inp["sel_bias"]))
+
+
+def _check_against_oracle(cfg, inp, xs, ys, slots):
+    """Every step's output against the oracle's forward, and the tier's counters
+    against the oracle's tier fed the same steps (each step asks for its active
+    experts in ascending order, the shared experts included)."""
+    nE = cfg.E + cfg.S
+    tier_o = oracle.TierOracle(min(slots, nE), nE)
+    Wg, Wu, Wd = (host(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    for x, y in zip(xs, ys):
+        y_ref, ids_ref, _ = oracle.forward(host(x), host(inp["Wr"]), Wg, Wu, Wd, cfg.k,
+                                           cfg.gate, S=cfg.S, **_oracle_kw(cfg, inp))
+        err = rel_err(host(y).double().numpy(), y_ref)
+        assert err <= y_tol(cfg), err
+        active = sorted(set(ids_ref.flatten().tolist()) | set(range(cfg.E, nE)))
+        tier_o.step(active)
+    return tier_o.stats()
 
 
 @pytest.mark.parametrize("slots", [49, 20, 7, 2, 1])
@@ -64,14 +98,19 @@ def test_tier_equals_resident_layer(slots):
     inp = make_inputs(cfg, seed=3, device=DEV)
     tier = _tier(cfg, inp, slots)
     assert tier.stats()["n_slots"] == min(slots, cfg.E + cfg.S)
-    for x in _xs(cfg, 5, seed=slots):
+    xs, ys = _xs(cfg, 5, seed=slots, inp=inp), []
+    for x in xs:
         y_ref, ids_ref = _resident(cfg, inp, x)
         ids = torch.empty_like(ids_ref)
         y = tier.forward(x, topk_ids=ids)
         assert moe.moe_get_device_status(tier.ws) == moe.MOE_OK
         assert torch.equal(ids, ids_ref)
         assert torch.equal(y, y_ref)
+        ys.append(y.clone())
     st = tier.stats()
+    ost = _check_against_oracle(cfg, inp, xs, ys, slots)
+    for key in ("hits", "misses", "evictions", "extra_passes", "resident"):
+        assert st[key] == ost[key], (key, st[key], ost[key])
     assert st["steps"] == 5 and st["resident"] <= st["n_slots"]
     assert st["bytes_loaded"] == st["misses"] * 3 * cfg.I * cfg.d * 2
     if slots < 10:  # a step's experts (up to 24 * 6 routed + 1 shared) exceed the slots
@@ -141,14 +180,19 @@ def test_tier_full_size_kimi_decode():
     inp = make_inputs(cfg, seed=0, device=DEV)
     nE = cfg.E + cfg.S
     tier = _tier(cfg, inp, nE // 4)
-    for x in _xs(cfg, 3, seed=0):
+    xs, ys = _xs(cfg, 3, seed=0, inp=inp), []
+    for x in xs:
         y_ref, ids_ref = _resident(cfg, inp, x)
         ids = torch.empty_like(ids_ref)
         y = tier.forward(x, topk_ids=ids)
         assert moe.moe_get_device_status(tier.ws) == moe.MOE_OK
         assert torch.equal(ids, ids_ref) and torch.equal(y, y_ref)
+        ys.append(y.clone())
     st = tier.stats()
     assert st["n_slots"] == nE // 4 and st["extra_passes"] > 0
+    ost = _check_against_oracle(cfg, inp, xs, ys, nE // 4)
+    for key in ("hits", "misses", "evictions", "extra_passes", "resident"):
+        assert st[key] == ost[key], (key, st[key], ost[key])
     tier.close()
     del inp
     torch.cuda.empty_cache()

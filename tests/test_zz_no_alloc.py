@@ -1,8 +1,10 @@
 """moe_expert_ffn_noalloc: the expert FFN for callers that cannot allocate
 device memory (their host application owns it all, or they must never call
-cudaMalloc).  It must give the results of moe_expert_ffn, which uses a caller
-workspace, call after call, although its scratch is one fixed array inside the
-library that every call reuses.  This file is collected last on purpose."""
+cudaMalloc).  It must give exactly the rows of moe_expert_ffn, which runs the
+same kernels with a caller workspace, call after call -- also after a call for
+another layer has left its own data in the one fixed array inside the library
+that every call reuses -- and those rows must match the oracle's per-expert
+FFN.  This file is collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -34,15 +36,30 @@ def _built():
     build.build()
 
 
-@pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
-def test_noalloc_matches_workspace_entry_point(cfg):
-    inp = enforce_margins(make_inputs(cfg, seed=13, device=DEV), cfg, 13)
+def _layer(cfg, seed):
+    """A layer's inputs and the oracle's dispatch plan of its routing."""
+    inp = enforce_margins(make_inputs(cfg, seed=seed, device=DEV), cfg, seed)
     ids, _ = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate,
                           norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling,
                           logit_bias=host(inp["logit_bias"]), sel_bias=host(inp["sel_bias"]))
     plan = oracle.plan(ids, cfg.E, cfg.S)
     off = torch.from_numpy(plan["expert_offsets"]).to(DEV)
     tok = torch.from_numpy(plan["token_indices"]).to(DEV)
+    return inp, plan, off, tok
+
+
+def _noalloc(cfg, inp, off, tok):
+    P = cfg.T * (cfg.k + cfg.S)
+    y = torch.full((P, cfg.d), float("nan"), dtype=cfg.torch_dtype, device=DEV)
+    moe.moe_expert_ffn_noalloc(moe.desc_from_config(cfg), inp["x"], off, tok, None, inp["Wg"],
+                               inp["Wu"], inp["Wd"], y)
+    torch.cuda.synchronize()
+    return y
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
+def test_noalloc_matches_workspace_entry_point(cfg):
+    inp, plan, off, tok = _layer(cfg, 13)
     desc = moe.desc_from_config(cfg)
     P = cfg.T * (cfg.k + cfg.S)
     # the existing entry point, with a workspace
@@ -50,16 +67,27 @@ def test_noalloc_matches_workspace_entry_point(cfg):
     y_ws = torch.zeros((P, cfg.d), dtype=cfg.torch_dtype, device=DEV)
     moe.moe_expert_ffn(desc, inp["x"], off, tok, None, inp["Wg"], inp["Wu"], inp["Wd"], y_ws, ws)
     torch.cuda.synchronize()
-    ref = host(y_ws).double().numpy()
-    assert np.isfinite(ref).all() and np.abs(ref).max() > 0
-    # the allocation-free one, twice in a row (the second call reuses the scratch)
-    for _ in range(2):
-        y_na = torch.full((P, cfg.d), float("nan"), dtype=cfg.torch_dtype, device=DEV)
-        moe.moe_expert_ffn_noalloc(desc, inp["x"], off, tok, None, inp["Wg"], inp["Wu"],
-                                   inp["Wd"], y_na)
-        torch.cuda.synchronize()
-        got = host(y_na).double().numpy()
-        assert rel_err(got, ref) <= y_tol(cfg), rel_err(got, ref)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    # both run the same kernels on the same plan: the rows must be identical
+    y1 = _noalloc(cfg, inp, off, tok)
+    assert torch.equal(y1, y_ws)
+    # another layer in between leaves different data in the shared scratch;
+    # the next call must not depend on it
+    other = CASES[(CASES.index(cfg) + 1) % len(CASES)]
+    o_inp, _, o_off, o_tok = _layer(other, 14)
+    _noalloc(other, o_inp, o_off, o_tok)
+    y2 = _noalloc(cfg, inp, off, tok)
+    assert torch.equal(y2, y_ws)
+    # and the rows against the oracle's per-expert FFN
+    o, t = plan["expert_offsets"], plan["token_indices"]
+    ref = np.zeros((P, cfg.d))
+    for e in range(cfg.E + cfg.S):
+        if o[e + 1] > o[e]:
+            ref[o[e]:o[e + 1]] = oracle.expert_rows(host(inp["x"]), host(inp["Wg"][e]),
+                                                    host(inp["Wu"][e]), host(inp["Wd"][e]),
+                                                    t[o[e]:o[e + 1]])
+    err = rel_err(host(y2).double().numpy(), ref)
+    assert err <= y_tol(cfg), err
 
 
 def test_noalloc_rejects_layers_beyond_its_scratch():
