@@ -543,6 +543,32 @@ def host_huge_fraction(nbytes):
     return None
 
 
+def percentiles(v):
+    """min / p10 / median / p90 / max of a list (None when empty)."""
+    if not v:
+        return None
+    v = sorted(v)
+    pick = lambda q: v[min(len(v) - 1, int(round(q * (len(v) - 1))))]
+    return {"n": len(v), "min": v[0], "p10": pick(0.1), "median": pick(0.5), "p90": pick(0.9),
+            "max": v[-1]}
+
+
+def load_summary(load_ms, load_bytes):
+    """The tier's load launches: their host -> HBM rate (GB/s) distribution, and
+    how many bytes moved in launches slower than half the median rate."""
+    rates = [b / (t / 1e3) / 1e9 for t, b in zip(load_ms, load_bytes) if t > 0 and b > 0]
+    if not rates:
+        return {"launches": len(load_ms), "gbs": None}
+    med = percentiles(rates)["median"]
+    slow = [(r, b) for r, b in zip(rates, load_bytes) if r < 0.5 * med]
+    total = sum(load_bytes)
+    return {"launches": len(rates), "bytes": total, "gbs": percentiles(rates),
+            "slow_launches": len(slow),
+            "slow_bytes_share": sum(b for _, b in slow) / total if total else 0.0,
+            "time_share_in_slow": (sum(b / (r * 1e9) for r, b in slow)
+                                   / sum(t / 1e3 for t in load_ms) if slow else 0.0)}
+
+
 def run_tier(args, rank, world):
     """The layer through the expert tier: expert projections in page-locked host
     memory, args.tier_slots expert slots in HBM.  Steps cycle through
@@ -591,13 +617,29 @@ def run_tier(args, rank, world):
     timed(lambda x: layer.forward(x, y=y), args.warmup)
     resident_ms = timed(lambda x: layer.forward(x, y=y), args.steps)
     link = host_link_gbs(dev)
+    touch = None
+    if args.tier_touch:  # read every expert's host memory from the GPU once, untimed
+        nE = cfg.E + cfg.S
+        n_slots = tier.stats()["n_slots"]
+        moe.moe_profile_enable(2)
+        t0 = time.perf_counter()
+        for e0 in range(0, nE, n_slots):
+            tier.prefetch(list(range(e0, min(nE, e0 + n_slots))))
+        torch.cuda.synchronize()
+        touch_s = time.perf_counter() - t0
+        t_ms, t_bytes = moe.moe_profile_list("load_experts")
+        moe.moe_profile_enable(False)
+        touch = {"seconds": touch_s, "loads": load_summary(t_ms, t_bytes)}
     timed(lambda x: tier.forward(x, y=y), args.warmup)
     s0 = tier.stats()
     sampler = ClockSampler(local)
     sampler.start()
     sampler.mark(True)
     launches0 = moe.moe_launch_count()
+    moe.moe_profile_enable(2)  # event pairs around the loads (on the tier's copy stream) only
     ms = timed(lambda x: tier.forward(x, y=y), args.steps)
+    timed_ms, timed_bytes = moe.moe_profile_list("load_experts")
+    moe.moe_profile_enable(False)
     launches = moe.moe_launch_count() - launches0
     sampler.mark(False)
     clocks = sampler.stop()
@@ -607,6 +649,17 @@ def run_tier(args, rank, world):
     K = args.steps
     d = {k: s1[k] - s0[k] for k in ("hits", "misses", "evictions", "extra_passes",
                                     "bytes_loaded")}
+    # ---- the same K steps again, now with every expert they need resident: the
+    # host's wall time per step (each step waits once on the host for its routing)
+    step_ms = []
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            t0 = time.perf_counter()
+            tier.forward(xs[i % len(xs)], y=y)
+            stream.synchronize()
+            step_ms.append((time.perf_counter() - t0) * 1e3)
+    link_after = host_link_gbs(dev)
+    loads = load_summary(timed_ms, timed_bytes)
     loaded = d["bytes_loaded"] / K
     bound_ms = resident_ms / K + loaded / (link * 1e9) * 1e3
     value = cfg.T * K / (ms / 1e3)
@@ -629,7 +682,11 @@ def run_tier(args, rank, world):
                  "misses_per_step": d["misses"] / K, "evictions_per_step": d["evictions"] / K,
                  "extra_passes_per_step": d["extra_passes"] / K,
                  "h2d_gbs_achieved": d["bytes_loaded"] / (ms / 1e3) / 1e9,
-                 "host_weights_in_huge_pages": huge},
+                 "host_weights_in_huge_pages": huge,
+                 "host_link_gbs_after": link_after,
+                 "loads_in_timed_region": loads,
+                 "host_memory_touched_first": touch,
+                 "repeat_step_wall_ms": percentiles(step_ms)},
         "gpu_launches": launches,
         "launch_mode": "direct (a host wait per step)",
         "clocks": clocks,
@@ -788,6 +845,9 @@ def main():
                          "expert slots (experts in host memory)")
     ap.add_argument("--tier-inputs", type=int, default=8,
                     help="token batches in rotation for --tier-slots")
+    ap.add_argument("--tier-touch", action="store_true",
+                    help="with --tier-slots: read every expert's host memory from the GPU once "
+                         "before the warm-up (prefetching all experts, slot-load by slot-load)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3  # the timing rules want at least three untimed steps

@@ -112,9 +112,11 @@ moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_E
 struct ProfRecord {
   std::string name;
   cudaEvent_t start, stop;
+  uint64_t bytes;  // bytes the launch moves, when its launcher states them (else 0)
 };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
+bool g_prof_bytes_only = false;  // record only launches that state the bytes they move
 std::vector<ProfRecord> g_prof;
 std::vector<cudaEvent_t> g_prof_free;
 std::atomic<long long> g_launches{0};
@@ -276,10 +278,11 @@ WsLayout ws_layout(const moe_layer_desc& D) {
   return L;
 }
 
-ProfScope::ProfScope(const char* n, cudaStream_t s) : name(n), stream(s), slot(-1) {
+ProfScope::ProfScope(const char* n, cudaStream_t s, uint64_t bytes)
+    : name(n), stream(s), slot(-1) {
   std::lock_guard<std::mutex> g(g_prof_mu);
-  if (!g_prof_on) return;
-  ProfRecord r{n, take_event(), take_event()};
+  if (!g_prof_on || (g_prof_bytes_only && bytes == 0)) return;
+  ProfRecord r{n, take_event(), take_event(), bytes};
   if (!r.start || !r.stop) return;
   if (cudaEventRecord(r.start, s) != cudaSuccess) return;
   g_prof.push_back(r);
@@ -1017,6 +1020,7 @@ moe_status moe_profile_enable(int on) {
   }
   g_prof.clear();
   g_prof_on = on != 0;
+  g_prof_bytes_only = on == 2;
   return MOE_OK;
 }
 
@@ -1035,6 +1039,27 @@ moe_status moe_profile_query(const char* kernel, int32_t* launches, float* total
   }
   *launches = n;
   *total_ms = tot;
+  return MOE_OK;
+}
+
+moe_status moe_profile_list(const char* kernel, int32_t max_n, float* ms, uint64_t* bytes,
+                            int32_t* n_out) {
+  if (!kernel || !n_out || max_n < 0 || (max_n > 0 && (!ms || !bytes)))
+    return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> g(g_prof_mu);
+  int n = 0;
+  for (auto& r : g_prof) {
+    if (r.name != kernel) continue;
+    if (n < max_n) {
+      if (cudaEventSynchronize(r.stop) != cudaSuccess) return MOE_ERR_CUDA;
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess) return MOE_ERR_CUDA;
+      ms[n] = t;
+      bytes[n] = r.bytes;
+    }
+    ++n;
+  }
+  *n_out = n;
   return MOE_OK;
 }
 

@@ -44,7 +44,7 @@ inline size_t dtype_size(int dt) { return dt == MOE_BF16 ? 2 : 4; }
 
 // ---------------------------------------------------------------- profiling hooks
 struct ProfScope {
-  ProfScope(const char* name, cudaStream_t s);
+  ProfScope(const char* name, cudaStream_t s, uint64_t bytes = 0);
   ~ProfScope();
   const char* name;
   cudaStream_t stream;

@@ -429,6 +429,7 @@ cudaError_t launch_load_experts(const ExpertLoadJobs& jobs, int n, const void* c
   if (n <= 0) return cudaSuccess;
   if (n > kMaxExpertLoadJobs || mat_bytes % 16) return cudaErrorInvalidValue;
   count_launch();
+  ProfScope pr("load_experts", s, (uint64_t)n * 3 * mat_bytes);
   load_experts_kernel<<<num_sms() * 4, 512, 0, s>>>(
       jobs, n, static_cast<const uint4*>(host[0]), static_cast<const uint4*>(host[1]),
       static_cast<const uint4*>(host[2]), static_cast<uint4*>(pool[0]),

@@ -9,7 +9,7 @@ status.  There is no fallback: if libmoe.so is missing, every call raises.
 Entry points carry the C names: moe_workspace_size, moe_workspace_init,
 moe_route, moe_plan_dispatch, moe_expert_ffn, moe_combine, moe_layer_forward,
 moe_get_device_status, moe_status_string, moe_launch_count,
-moe_profile_enable, moe_profile_query, the Q8_0 and no-alloc variants, the
+moe_profile_enable, moe_profile_query, moe_profile_list, the Q8_0 and no-alloc variants, the
 slot cache (moe_slot_cache_*) and the expert tier (moe_tier_*).
 """
 from __future__ import annotations
@@ -39,6 +39,7 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_init", "moe_route", "moe_plan_d
             "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_get_device_status",
             "moe_status_string", "moe_launch_count", "moe_profile_enable", "moe_profile_query",
             "moe_expert_ffn_noalloc", "moe_combine_partial", "moe_partial_missing_pairs",
+            "moe_profile_list",
             "moe_quantize_q8_0",
             "moe_expert_ffn_q8", "moe_layer_forward_q8", "moe_slot_cache_create",
             "moe_slot_cache_destroy", "moe_slot_cache_assign", "moe_slot_cache_slot_of",
@@ -150,6 +151,8 @@ def lib():
     L.moe_profile_enable.argtypes = [i32]
     L.moe_profile_query.argtypes = [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int32),
                                     ctypes.POINTER(ctypes.c_float)]
+    L.moe_profile_list.argtypes = [ctypes.c_char_p, ctypes.c_int32, vp, vp,
+                                   ctypes.POINTER(ctypes.c_int32)]
     for f in EXPORTED:
         if f not in ("moe_status_string", "moe_launch_count"):
             getattr(L, f).restype = ctypes.c_int
@@ -458,8 +461,11 @@ def moe_launch_count() -> int:
     return lib().moe_launch_count()
 
 
-def moe_profile_enable(on: bool):
-    _check(lib().moe_profile_enable(1 if on else 0), "moe_profile_enable")
+def moe_profile_enable(on):
+    """True / 1: record every launch; 2: only launches that state their bytes
+    (the expert tier's loads); False / 0: stop."""
+    mode = 2 if on == 2 else (1 if on else 0)
+    _check(lib().moe_profile_enable(mode), "moe_profile_enable")
 
 
 def moe_profile_query(kernel: str):
@@ -469,6 +475,21 @@ def moe_profile_query(kernel: str):
     _check(lib().moe_profile_query(kernel.encode(), ctypes.byref(n), ctypes.byref(ms)),
            "moe_profile_query")
     return n.value, ms.value
+
+
+def moe_profile_list(kernel: str):
+    """The named kernel's recorded launches in launch order: (ms list, bytes list)."""
+    n = ctypes.c_int32(0)
+    _check(lib().moe_profile_list(kernel.encode(), 0, None, None, ctypes.byref(n)),
+           "moe_profile_list")
+    if n.value == 0:
+        return [], []
+    ms = (ctypes.c_float * n.value)()
+    by = (ctypes.c_uint64 * n.value)()
+    _check(lib().moe_profile_list(kernel.encode(), n.value, ctypes.cast(ms, ctypes.c_void_p),
+                                  ctypes.cast(by, ctypes.c_void_p), ctypes.byref(n)),
+           "moe_profile_list")
+    return list(ms), list(by)
 
 
 # ---------------------------------------------------------------- slot cache and expert tier

@@ -441,15 +441,25 @@ int64_t moe_launch_count(void);
 
 /* Profiling.  moe_profile_enable(1) starts recording a CUDA event pair around
    every kernel this library launches (on the launching stream) and clears
-   earlier records; moe_profile_enable(0) stops.  moe_profile_query()
+   earlier records; moe_profile_enable(2) does the same for the launches that
+   state the bytes they move only (the expert tier's loads), so the other
+   kernels' streams get no extra events; moe_profile_enable(0) stops.  moe_profile_query()
    synchronizes on the recorded events and returns, for the named kernel, the
    number of recorded launches and their summed device time in milliseconds.
    Kernel names: router_logits_splitk, router_logits_tc, router_topk,
    plan_small, plan_mark, plan_scan, plan_place, gather_rows, scatter_rows,
    ffn_gateup_simt, ffn_down_simt, ffn_gateup_tc, ffn_down_tc,
-   ffn_gateup_tc_q8, ffn_down_tc_q8, quantize_q8_0, combine, combine_partial. */
+   ffn_gateup_tc_q8, ffn_down_tc_q8, quantize_q8_0, combine, combine_partial,
+   missing_pairs, load_experts (the expert tier's loads of host-resident
+   experts into HBM slots).
+   moe_profile_list() gives the named kernel's recorded launches one by one,
+   in launch order: the first max_n durations (ms) and the bytes each launch
+   moves where its launcher states them (load_experts: the experts' three
+   projections; 0 otherwise); *n_out = the number of recorded launches. */
 moe_status moe_profile_enable(int on);
 moe_status moe_profile_query(const char* kernel, int32_t* launches, float* total_ms);
+moe_status moe_profile_list(const char* kernel, int32_t max_n, float* ms, uint64_t* bytes,
+                            int32_t* n_out);
 
 #ifdef __cplusplus
 }

@@ -196,3 +196,25 @@ def test_tier_full_size_kimi_decode():
     tier.close()
     del inp
     torch.cuda.empty_cache()
+
+
+def test_load_launches_are_profiled_with_their_bytes():
+    """moe_profile_list gives each load launch of the tier with the bytes it
+    moved; they add up to the tier's bytes_loaded counter."""
+    cfg = SMALL
+    inp = make_inputs(cfg, seed=8, device=DEV)
+    tier = _tier(cfg, inp, 7)
+    s0 = tier.stats()
+    moe.moe_profile_enable(True)
+    for x in _xs(cfg, 3, seed=4):
+        tier.forward(x)
+    torch.cuda.synchronize()
+    ms, nbytes = moe.moe_profile_list("load_experts")
+    g_ms, g_bytes = moe.moe_profile_list("ffn_gateup_tc")
+    moe.moe_profile_enable(False)
+    s1 = tier.stats()
+    assert len(ms) > 0 and all(t > 0 for t in ms)
+    assert sum(nbytes) == s1["bytes_loaded"] - s0["bytes_loaded"]
+    assert all(b % (3 * cfg.I * cfg.d * 2) == 0 for b in nbytes)
+    assert len(g_ms) >= 3 and all(b == 0 for b in g_bytes)
+    tier.close()
