@@ -92,6 +92,11 @@ struct CfgQ8 {
   static_assert(COLS <= 512, "TMEM columns");
   static_assert(WS <= 32 && TS <= 32, "stages in flight tracked in 32-bit masks");
   static_assert(NI >= 1 && NI <= 4, "issuers");
+  // K block j goes to issuer j % NI and to token / converted stage j % TS / j % CS:
+  // with TS and CS multiples of NI every stage is only ever taken by one issuer,
+  // so no issuer can run a full phase ahead of a stage another issuer still
+  // holds (its parity wait would then see the older phase complete)
+  static_assert(TS % NI == 0 && CS % NI == 0, "ring stages per issuer");
   static_assert(SMEM_TOTAL <= 232448, "shared memory");
 };
 
