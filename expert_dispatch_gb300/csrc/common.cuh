@@ -63,6 +63,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Orders this thread's earlier generic-proxy accesses to shared memory (plain
+// loads and stores) before later async-proxy accesses (TMA copies, tcgen05).
+// A thread that reads a buffer a TMA copy then refills runs this after its
+// reads and before the barrier that hands the buffer back.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

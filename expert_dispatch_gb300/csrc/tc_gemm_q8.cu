@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
           ok = false;
           break;
         }
-        const uint8_t* __restrict__ w = smem + ws * C::W_BYTES;
+        const uint8_t* w = smem + ws * C::W_BYTES;
         uint4 codes[NCH];
         __half sh[NCH / 2];
 #pragma unroll
@@ -366,7 +366,12 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
 #pragma unroll
         for (int b = 0; b < NCH / 2; ++b)
           sh[b] = *reinterpret_cast<const __half*>(w + scale_off + b * 256);
-        __syncwarp();  // the warp's reads of the stage are done: hand it back
+        // hand the stage back as soon as it is read: the loader's next copy into
+        // it (an async-proxy write) may follow at once, so every lane orders its
+        // reads before it with a proxy fence (without one, rows of a tile were
+        // seen decoded from the next stage's data under light HBM load)
+        fence_proxy_async_shared();
+        __syncwarp();
         if (lane == 0) mbar_arrive(w_empty(ws));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {

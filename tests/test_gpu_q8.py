@@ -127,6 +127,63 @@ def test_layer_forward_q8_full_size(cfg):
     check_all_tokens(y_host, y_ref, ids_ref, cfg, 1e-2)
 
 
+def tile_covering_tokens(plan, tile_rows, rng):
+    """Tokens such that every tile of every expert's batch, for each tile height
+    in tile_rows, holds at least one of their rows (one random row per tile)."""
+    o, tok = plan["expert_offsets"], plan["token_indices"]
+    picked = set()
+    for e in range(len(o) - 1):
+        cnt = int(o[e + 1] - o[e])
+        for bt in tile_rows:
+            for s0 in range(0, cnt, bt):
+                picked.add(int(tok[o[e] + s0 + rng.integers(0, min(bt, cnt - s0))]))
+    return np.array(sorted(picked), np.int32)
+
+
+@pytest.mark.parametrize("name", ["deepseek_prefill", "skewed_zipf"])
+def test_layer_forward_q8_full_size_prefill(name):
+    """The prefill workloads at full size on Q8_0 experts (the 192-token gate/up
+    and 256-token down variants), checked on a token sample that puts at least
+    one checked row in every tile of every expert's batch at both tile heights.
+    Oracle side: per active expert, its dequantized projections over the sampled
+    tokens' rows of its batch (oracle.expert_rows), combined per token with the
+    oracle's gate weights -- one expert's fp64 weights in memory at a time."""
+    cfg = CONFIGS[name]
+    inp = enforce_margins(make_inputs(cfg, seed=0, device=DEV), cfg, 0)
+    desc = moe.desc_from_config(cfg)
+    Wg, Wu, Wd = (moe.quantize_q8_0(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    layer = moe.MoeLayer(desc, inp["Wr"], Wg, Wu, Wd, logit_bias=inp["logit_bias"],
+                         sel_bias=inp["sel_bias"])
+    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    y = layer.forward(inp["x"], topk_ids=ids)
+    assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
+    y_host = host(y).double().numpy()
+    del layer, Wg, Wu, Wd, y
+    torch.cuda.empty_cache()
+    kw = dict(norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling,
+              logit_bias=host(inp["logit_bias"]), sel_bias=host(inp["sel_bias"]))
+    ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate, **kw)
+    np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
+    plan = oracle.plan(ids_ref, cfg.E, cfg.S)
+    tokens = tile_covering_tokens(plan, (192, 256), np.random.default_rng(3))
+    o, tok = plan["expert_offsets"], plan["token_indices"]
+    want = np.zeros(cfg.T, bool)
+    want[tokens] = True
+    P = cfg.T * (cfg.k + cfg.S)
+    rows = np.zeros((P, cfg.d))
+    x_host = host(inp["x"])
+    for e in range(cfg.E + cfg.S):
+        r = np.arange(o[e], o[e + 1])
+        r = r[want[tok[r]]]  # the batch rows of sampled tokens
+        if len(r) == 0:
+            continue
+        dg, du, dd = (_oracle_deq(inp[n][e:e + 1])[0] for n in ("Wg", "Wu", "Wd"))
+        rows[r] = oracle.expert_rows(x_host, dg, du, dd, tok[r])
+    sr = plan["slot_row"][tokens]
+    y_ref = oracle.combine(rows, sr, cfg.k, cfg.S, w=w_ref[tokens])
+    check_all_tokens(y_host[tokens], y_ref, ids_ref[tokens], cfg, 1e-2)
+
+
 # Batch sizes on the tile edges of the Q8_0 kernels: 32-token tiles with
 # several issuers (mean batch <= 48 rows), and the large-batch variants
 # (192-token gate/up, 256-token down), with weight blocks that end inside a

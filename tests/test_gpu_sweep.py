@@ -252,3 +252,59 @@ def test_combine_partial_random_sweep(seed):
     n = int(host(n_pairs)[0])
     assert n == len(want)
     np.testing.assert_array_equal(host(pairs).numpy()[:n], want)
+
+
+def _draw_medium(seed):
+    """Medium layers: K of 512-1024 (the large-tile kernels at longer reductions
+    than the small draws reach), 256-2048 tokens, one or two tile heights of
+    rows per expert, skewed or uniform routing."""
+    rng = np.random.default_rng(70000 + seed)
+    E = int(rng.integers(4, 9)) if rng.random() < 0.35 else int(rng.integers(8, 65))
+    k = int(rng.integers(2, min(E, 8) + 1))
+    S = int(rng.integers(0, 2))
+    T = int(rng.integers(256, 2049))
+    gate = int(rng.integers(0, 2))
+    d, I = 64 * int(rng.integers(8, 17)), 64 * int(rng.integers(8, 17))
+    return LayerConfig("medium_%d" % seed, T=T, d=d, E=E, I=I, k=k, S=S, gate=gate,
+                       norm_topk=gate, routed_scaling=2.5 if gate else 1.0,
+                       sel_bias_range=0.1 if gate else 0.0,
+                       zipf_s=1.2 if rng.random() < 0.5 else 0.0)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("seed", range(6))
+def test_layer_medium_sweep_every_token(seed):
+    """Medium layers, bf16 and Q8_0 experts: routing bit-exact and every token's
+    output against the oracle (Q8_0: the oracle on its own dequantization of the
+    same weights)."""
+    from tests.helpers import check_all_tokens
+    cfg = _draw_medium(seed)
+    try:
+        inp = make_case(cfg, seed=seed, device=DEV)
+    except RuntimeError as e:
+        pytest.skip(str(e))
+    kw = dict(norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling,
+              logit_bias=host(inp["logit_bias"]), sel_bias=host(inp["sel_bias"]))
+    desc = moe.desc_from_config(cfg)
+    ids_ref, w_ref = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate, **kw)
+    for q8 in (False, True):
+        Wg, Wu, Wd = inp["Wg"], inp["Wu"], inp["Wd"]
+        if q8:
+            Wg, Wu, Wd = (moe.quantize_q8_0(W) for W in (Wg, Wu, Wd))
+        layer = moe.MoeLayer(desc, inp["Wr"], Wg, Wu, Wd, logit_bias=inp["logit_bias"],
+                             sel_bias=inp["sel_bias"])
+        ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+        w = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
+        y = layer.forward(inp["x"], topk_ids=ids, topk_w=w)
+        assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
+        np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
+        check_weights(host(w).numpy(), w_ref, inp, cfg)
+        if q8:
+            ref_w = [list(_deq(inp[n])) for n in ("Wg", "Wu", "Wd")]
+            y_ref, _, _ = oracle.forward(host(inp["x"]), oracle.widen(host(inp["Wr"])), *ref_w,
+                                         cfg.k, cfg.gate, S=cfg.S, **kw)
+        else:
+            y_ref, _, _ = oracle.forward(host(inp["x"]), host(inp["Wr"]), host(inp["Wg"]),
+                                         host(inp["Wu"]), host(inp["Wd"]), cfg.k, cfg.gate,
+                                         S=cfg.S, **kw)
+        check_all_tokens(host(y).double().numpy(), y_ref, ids_ref, cfg, 1e-2)
