@@ -14,7 +14,9 @@
 //   * the token loader (warp 2) brings the unit's token rows (fp16, 128-byte
 //     swizzle) into a token stage (TS deep);
 //   * converter warps read the codes and scales into registers and hand the
-//     weight stage straight back, then decode each of its K blocks in turn:
+//     weight stage straight back (each lane first fences its reads against
+//     the loader's next TMA copy into the stage: different proxies), then
+//     decode each of its K blocks in turn:
 //     scale * q rounded to fp16.
 //     The MMA takes its M-side operand from tensor memory (one weight row per
 //     TMEM lane, two 16-bit K elements per 32-bit column), so each converter
