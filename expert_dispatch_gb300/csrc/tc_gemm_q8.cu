@@ -13,10 +13,10 @@
 //     down GEMM, one operand per stage, measured ~10 % slower);
 //   * the token loader (warp 2) brings the unit's token rows (fp16, 128-byte
 //     swizzle) into a token stage (TS deep);
-//   * converter warps read the codes and scales into registers and hand the
-//     weight stage straight back (each lane first fences its reads against
-//     the loader's next TMA copy into the stage: different proxies), then
-//     decode each of its K blocks in turn:
+//   * converter warps read the codes and scales into registers, decode the
+//     stage's first K block and hand the weight stage back (each lane first
+//     fences its reads against the loader's next TMA copy into the stage:
+//     different proxies), then decode the second:
 //     scale * q rounded to fp16.
 //     The MMA takes its M-side operand from tensor memory (one weight row per
 //     TMEM lane, two 16-bit K elements per 32-bit column), so each converter
@@ -30,9 +30,9 @@
 //     two waits, a fence and two commits), so NI issuers (2 for gate/up, 4
 //     for down) take K block j of each unit when j % NI is theirs, into NI
 //     partial accumulators that the epilogue adds.
-// A weight stage is thus held only from its TMA to the converters' loads,
-// so the in-flight depth of the weight stream does not shrink by the decode
-// and MMA latency; the weight loader never waits for the predecessor grid
+// A weight stage is thus held only from its TMA until the converters have
+// decoded its first K block, so the in-flight depth of the weight stream does
+// not shrink by the MMA latency; the weight loader never waits for the predecessor grid
 // (weights are never written by the kernel just before; the token rows are,
 // so the token loader waits).  The 128-byte swizzle puts 16-byte chunk j of
 // code row r at chunk j ^ (r % 8), so a warp's 32 rows read one chunk each
@@ -368,13 +368,17 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
 #pragma unroll
         for (int b = 0; b < NCH / 2; ++b)
           sh[b] = *reinterpret_cast<const __half*>(w + scale_off + b * 256);
-        // hand the stage back as soon as it is read: the loader's next copy into
-        // it (an async-proxy write) may follow at once, so every lane orders its
-        // reads before it with a proxy fence (without one, rows of a tile were
-        // seen decoded from the next stage's data under light HBM load)
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(w_empty(ws));
+        // The stage goes back to the loader once its first K block is decoded
+        // (every code and scale is in registers by then).  The loader's next
+        // copy into it is an async-proxy write, so every lane first orders its
+        // reads before it with a proxy fence: without one, rows of a tile were
+        // seen decoded from the next stage's data under light HBM load.  Placed
+        // after the first block's decode, the fence waits for nothing.
+        auto hand_back = [&] {
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(w_empty(ws));
+        };
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (h >= nk) break;
@@ -407,6 +411,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(conv_full(cs));
           ++kcount;
+          if (h == 0) hand_back();
         }
       }
     }
