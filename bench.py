@@ -498,7 +498,11 @@ def run_gpu(args, rank, world):
         "e2e": rec["e2e"],
         "gpu_launches": rec["gpu_launches"],
         "launch_mode": rec["launch_mode"],
-        "kernel_timing": "event pair per launch over %d directly launched steps" % args.steps,
+        "kernel_timing": ("event pair per launch over %d directly launched steps; each workload's "
+                          "kernel_event_sum_ms_per_step exceeds its graph-replayed ms_per_step by the "
+                          "event pairs' own cost and by the overlap of neighbouring kernels "
+                          "(programmatic dependent launch) that event-bracketed launches lose"
+                          % args.steps),
         "clocks": rec["clocks"],
         "published_context": PUBLISHED_CONTEXT,
     }
