@@ -127,6 +127,27 @@ def test_layer_forward_q8_full_size(cfg):
     check_all_tokens(y_host, y_ref, ids_ref, cfg, 1e-2)
 
 
+def test_layer_forward_q8_max_groups():
+    """The largest layer record on Q8_0 experts: 1024 routed experts, top-32 and
+    4 shared experts (1028 expert batches, the kernels' schedule limit), every
+    token against the oracle on the dequantized weights."""
+    cfg = LayerConfig("q_max_groups", T=40, d=128, E=1024, I=64, k=32, S=4, norm_topk=1)
+    inp = enforce_margins(make_inputs(cfg, seed=7, device=DEV), cfg, 7)
+    desc = moe.desc_from_config(cfg)
+    Wg, Wu, Wd = (moe.quantize_q8_0(inp[n]) for n in ("Wg", "Wu", "Wd"))
+    layer = moe.MoeLayer(desc, inp["Wr"], Wg, Wu, Wd)
+    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    y = layer.forward(inp["x"], topk_ids=ids)
+    assert moe.moe_get_device_status(layer.ws) == moe.MOE_OK
+    kw = dict(norm_topk=cfg.norm_topk, routed_scaling=cfg.routed_scaling)
+    ids_ref, _ = oracle.route(host(inp["x"]), host(inp["Wr"]), cfg.k, cfg.gate, **kw)
+    np.testing.assert_array_equal(host(ids).numpy(), ids_ref)
+    deq = [list(_oracle_deq(inp[n])) for n in ("Wg", "Wu", "Wd")]
+    y_ref, _, _ = oracle.forward(host(inp["x"]), oracle.widen(host(inp["Wr"])), *deq, cfg.k,
+                                 cfg.gate, S=cfg.S, **kw)
+    check_all_tokens(host(y).double().numpy(), y_ref, ids_ref, cfg, 1e-2)
+
+
 def tile_covering_tokens(plan, tile_rows, rng):
     """Tokens such that every tile of every expert's batch, for each tile height
     in tile_rows, holds at least one of their rows (one random row per tile)."""
