@@ -473,9 +473,17 @@ def run_gpu(args, rank, world):
             cfg = workload(name, args.T, args.E)
             is_head = (name == head_name and weights == head_weights)
             budget = args.cpu_budget if (is_head and want_cpu and weights == "dense") else None
-            m = measure_workload(cfg, args, weights, rank, world, dev, cpu_budget=budget)
-            rec = workload_record(cfg, m, weights, args, world, dev, pk, src)
             key = name if weights == "dense" else name + "+q8_0"
+            try:
+                m = measure_workload(cfg, args, weights, rank, world, dev, cpu_budget=budget)
+                rec = workload_record(cfg, m, weights, args, world, dev, pk, src)
+            except Exception as e:  # noqa: BLE001 -- the headline (measured first) must not be lost
+                if is_head or world > 1:
+                    raise
+                records[key] = {"workload": cfg.name, "expert_weights": weights,
+                                "error": "%s: %s" % (type(e).__name__, str(e)[:300])}
+                torch.cuda.empty_cache()
+                continue
             records[key] = rec
             if is_head:
                 head = (cfg, m, rec)
@@ -808,16 +816,21 @@ def run_reference(args, rank, world):
             if name == head_name:
                 continue
             wcfg = workload(name, args.T, args.E)
-            inp = make_inputs(wcfg, seed=args.seed, device=dev)
-            case = OracleCase(wcfg, inp)
-            del inp
-            n0 = min(wcfg.T, max(1, cores // 2))
-            t0 = case.time(case.sample(n0, 0))
-            nn = int(min(wcfg.T, max(n0, n0 * 3.0 / max(t0, 1e-3))))
-            tt = case.time(case.sample(nn, 1)) if nn > n0 else t0
-            recs[name] = {"workload": wcfg.name, "tokens_per_s": nn / tt, "cores": cores,
-                          "sample": "%d of the workload's %d tokens (%.1f s)" % (nn, wcfg.T, tt)}
-            del case
+            try:
+                inp = make_inputs(wcfg, seed=args.seed, device=dev)
+                case = OracleCase(wcfg, inp)
+                del inp
+                n0 = min(wcfg.T, max(1, cores // 2))
+                t0 = case.time(case.sample(n0, 0))
+                nn = int(min(wcfg.T, max(n0, n0 * 3.0 / max(t0, 1e-3))))
+                tt = case.time(case.sample(nn, 1)) if nn > n0 else t0
+                recs[name] = {"workload": wcfg.name, "tokens_per_s": nn / tt, "cores": cores,
+                              "sample": "%d of the workload's %d tokens (%.1f s)"
+                                        % (nn, wcfg.T, tt)}
+                del case
+            except Exception as e:  # noqa: BLE001 -- the headline line still prints
+                recs[name] = {"workload": wcfg.name, "error": "%s: %s" % (type(e).__name__,
+                                                                          str(e)[:300])}
             if dev == "cuda":
                 torch.cuda.empty_cache()
         out["workloads"] = recs
