@@ -29,7 +29,10 @@
 //     issues at most one MMA per ~45 cycles, and each K block also costs it
 //     two waits, a fence and two commits), so NI issuers (2 for gate/up, 4
 //     for down) take K block j of each unit when j % NI is theirs, into NI
-//     partial accumulators that the epilogue adds.
+//     partial accumulators that the epilogue adds.  The large-tile gate/up
+//     has no TMEM for partial sets; there two issuers split the operands
+//     instead (gate MMAs on one thread, up MMAs on the other), because each
+//     issuer's waits stall it until its own MMAs drain.
 // A weight stage is thus held only from its TMA until the converters have
 // decoded its first K block, so the in-flight depth of the weight stream does
 // not shrink by the MMA latency; the weight loader never waits for the predecessor grid
@@ -63,9 +66,14 @@ constexpr int kFirstConvWarp = kFirstEpiWarp + tc::kEpiWarps;
 constexpr int kIssuer2 = kFirstConvWarp + kConvWarps;  // issuers 2 .. NI: warps kIssuer2 ..
 constexpr int threads_q8(int NI) { return 32 * (kIssuer2 + NI - 1); }
 
-template <int MODE, int BN, int WS, int TS, int CS, int NI>
+template <int MODE, int BN, int WS, int TS, int CS, int NI, bool OPS>
 struct CfgQ8 {
   static constexpr int NA = MODE == MODE_GATEUP ? 2 : 1;  // weight operands per K block
+  // NI issuers either split the K blocks of a unit (each into partial
+  // accumulators of its own, added by the epilogue) or, with OPS, take one
+  // operand each (gate / up) of every K block
+  static constexpr int NPART = OPS ? 1 : NI;  // partial accumulator sets
+  static constexpr int NCB = OPS ? 2 : 1;     // converted-stage barrier pairs per stage
   static constexpr int QA_BYTES = 128 * 128;  // int8 codes of a weight tile: 128 rows x two K blocks
   static constexpr int SA_BYTES = 4 * 128 * 2;  // its f16 scales [4 blocks][128 rows]
   static constexpr int SA_OFF = NA * QA_BYTES;            // scales inside a weight stage
@@ -79,13 +87,15 @@ struct CfgQ8 {
   // four convert alternate K blocks concurrently
   static constexpr int CONV_PER_BLOCK = NA == 2 ? kConvWarps : kConvWarps / 2;
   static constexpr int A_COLS = NA * 32 * CS;             // TMEM columns of the converted ring
-  static constexpr int NBUF = 2 * NI * NACC * BN + A_COLS <= 512 ? 2 : 1;
-  static constexpr int ACC_COLS = NBUF * NI * NACC * BN;  // [buffer][issuer][operand][BN]
+  // converter warps arriving on one converted-stage barrier
+  static constexpr int CONV_ARRIVALS = OPS ? kConvWarps / 2 : CONV_PER_BLOCK;
+  static constexpr int NBUF = 2 * NPART * NACC * BN + A_COLS <= 512 ? 2 : 1;
+  static constexpr int ACC_COLS = NBUF * NPART * NACC * BN;  // [buffer][part][operand][BN]
   static constexpr int COLS = ACC_COLS + A_COLS;
   static constexpr int TMEM_COLS =
       COLS <= 32 ? 32 : COLS <= 64 ? 64 : COLS <= 128 ? 128 : COLS <= 256 ? 256 : 512;
   static constexpr int BAR_OFF = T_OFF + TS * B_BYTES;
-  static constexpr int NBARS = 2 * WS + 2 * TS + 2 * CS + 2 * NBUF + 1;
+  static constexpr int NBARS = 2 * WS + 2 * TS + 2 * CS * NCB + 2 * NBUF + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
   static constexpr int PREFIX_OFF = MISC_OFF + 16;
   static constexpr int GSTART_OFF = PREFIX_OFF + 4 * (tc::kMaxGroups + 1);
@@ -94,11 +104,15 @@ struct CfgQ8 {
   static_assert(COLS <= 512, "TMEM columns");
   static_assert(WS <= 32 && TS <= 32, "stages in flight tracked in 32-bit masks");
   static_assert(NI >= 1 && NI <= 4, "issuers");
-  // K block j goes to issuer j % NI and to token / converted stage j % TS / j % CS:
-  // with TS and CS multiples of NI every stage is only ever taken by one issuer,
-  // so no issuer can run a full phase ahead of a stage another issuer still
-  // holds (its parity wait would then see the older phase complete)
-  static_assert(TS % NI == 0 && CS % NI == 0, "ring stages per issuer");
+  static_assert(!OPS || (NA == 2 && NI == 2), "operand split: one issuer per gate/up operand");
+  // K split: K block j goes to issuer j % NI and to token / converted stage
+  // j % TS / j % CS.  With TS and CS multiples of NI every stage is only ever
+  // taken by one issuer, so no issuer can run a full phase ahead of a stage
+  // another issuer still holds (its parity wait would then see the older
+  // phase complete).  Operand split: both issuers take every token stage, which
+  // is refilled only after both have released it, so neither can run a phase
+  // ahead; each converted-stage barrier has one issuer.
+  static_assert(OPS || (TS % NI == 0 && CS % NI == 0), "ring stages per issuer");
   static_assert(SMEM_TOTAL <= 232448, "shared memory");
 };
 
@@ -122,7 +136,7 @@ __device__ __forceinline__ uint4 dequant8_f16(uint2 codes, __half2 scale2) {
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-template <int MODE, int BN, int WS, int TS, int CS, int NI>
+template <int MODE, int BN, int WS, int TS, int CS, int NI, bool OPS>
 __global__ void __launch_bounds__(threads_q8(NI), 1)
     tc_grouped_gemm_q8(const __grid_constant__ CUtensorMap tmQ0,
                        const __grid_constant__ CUtensorMap tmQ1,
@@ -130,7 +144,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
                        const __grid_constant__ CUtensorMap tmS1,
                        const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmBfull, const Params p) {
-  using C = CfgQ8<MODE, BN, WS, TS, CS, NI>;
+  using C = CfgQ8<MODE, BN, WS, TS, CS, NI, OPS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -140,9 +154,12 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
   auto w_empty = [&](int s) { return bar0 + 8u * (WS + s); };
   auto t_full = [&](int s) { return bar0 + 8u * (2 * WS + s); };
   auto t_empty = [&](int s) { return bar0 + 8u * (2 * WS + TS + s); };
-  auto conv_full = [&](int s) { return bar0 + 8u * (2 * WS + 2 * TS + s); };
-  auto conv_empty = [&](int s) { return bar0 + 8u * (2 * WS + 2 * TS + CS + s); };
-  const uint32_t accf0 = bar0 + 8u * (2 * WS + 2 * TS + 2 * CS);
+  // converted stage s of operand set b (b = the operand with OPS, else 0)
+  auto conv_full = [&](int s, int b) { return bar0 + 8u * (2 * WS + 2 * TS + s * C::NCB + b); };
+  auto conv_empty = [&](int s, int b) {
+    return bar0 + 8u * (2 * WS + 2 * TS + (CS + s) * C::NCB + b);
+  };
+  const uint32_t accf0 = bar0 + 8u * (2 * WS + 2 * TS + 2 * CS * C::NCB);
   const uint32_t acce0 = accf0 + 8u * C::NBUF;
   const uint32_t drain_bar = acce0 + 8u * C::NBUF;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
@@ -162,12 +179,13 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
     }
     for (int s = 0; s < TS; ++s) {
       mbar_init(t_full(s), 1);
-      mbar_init(t_empty(s), 1);
+      mbar_init(t_empty(s), OPS ? 2 : 1);
     }
-    for (int s = 0; s < CS; ++s) {
-      mbar_init(conv_full(s), C::CONV_PER_BLOCK);
-      mbar_init(conv_empty(s), 1);
-    }
+    for (int s = 0; s < CS; ++s)
+      for (int b = 0; b < C::NCB; ++b) {
+        mbar_init(conv_full(s, b), C::CONV_ARRIVALS);
+        mbar_init(conv_empty(s, b), 1);
+      }
     for (int b = 0; b < C::NBUF; ++b) {
       mbar_init(accf0 + 8u * b, NI);
       mbar_init(acce0 + 8u * b, tc::kEpiWarps);
@@ -270,9 +288,15 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
     }
   } else if (warp == 1 || warp >= kIssuer2) {
     // ------------------------------------------------------------ MMA issuer(s)
-    // Issuer i takes the K blocks kb of each unit with (kb - kb0) % NI == i
-    // into its own partial accumulators; every issuer commits each unit's
-    // accumulators (accf counts NI arrivals) and the final drain.
+    // K split: issuer i takes the K blocks kb of each unit with
+    // (kb - kb0) % NI == i into its own partial accumulators.  Operand split:
+    // issuer i issues operand i's MMAs of every K block.  Every issuer commits
+    // each unit's accumulators (accf counts NI arrivals) and the final drain.
+    // A thread that has issued tcgen05.mma and then waits on an mbarrier (or
+    // reads shared memory at all) stalls until its queued MMAs have drained:
+    // ~260 SM cycles per K block, measured with back-to-back M=128 K=16 MMAs,
+    // against 4 x N/2 cycles of MMA work per operand.  Two issuers fill each
+    // other's stalls: the operand split made the 192-token gate/up ~6 % faster.
     const int me = warp == 1 ? 0 : warp - kIssuer2 + 1;
     if (lane == 0 && me < NI) {
       int it = 0;
@@ -285,12 +309,15 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
         const uint32_t use = C::NBUF == 2 ? (uint32_t)(it >> 1) : (uint32_t)it;
         if (!mbar_wait(acce0 + 8u * buf, (use & 1u) ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + (uint32_t)((buf * NI + me) * C::NACC * BN);
+        const uint32_t d0 =
+            OPS ? tmem_base + (uint32_t)((buf * C::NACC + me) * BN)
+                : tmem_base + (uint32_t)((buf * NI + me) * C::NACC * BN);
+        const int cb = OPS ? me : 0;
         bool ok = true;
         for (int kb = t.kb0; kb < t.kb1; ++kb, ++kcount) {
-          if ((kb - t.kb0) % NI != me) continue;
+          if (!OPS && (kb - t.kb0) % NI != me) continue;
           const int ts = kcount % TS, cs = kcount % CS;
-          if (!mbar_wait(conv_full(cs), (kcount / CS) & 1u, abort_flag, p.err) ||
+          if (!mbar_wait(conv_full(cs, cb), (kcount / CS) & 1u, abort_flag, p.err) ||
               !mbar_wait(t_full(ts), (kcount / TS) & 1u, abort_flag, p.err)) {
             ok = false;
             break;
@@ -299,16 +326,17 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
           const uint32_t sB = sbase + C::T_OFF + ts * C::B_BYTES;
           // operand op of converted stage cs: columns ACC_COLS + (cs * NA + op) * 32,
           // 8 columns per K=16 step
-          const uint32_t tA = tmem_base + (uint32_t)(C::ACC_COLS + cs * C::NA * 32);
+          const uint32_t tA =
+              tmem_base + (uint32_t)(C::ACC_COLS + cs * C::NA * 32 + (OPS ? me * 32 : 0));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bdesc = smem_desc_sw128(sB + kk * 32);
-            const uint32_t acc = (kb - t.kb0 >= NI || kk != 0) ? 1u : 0u;
+            const uint32_t acc = (kb - t.kb0 >= (OPS ? 1 : NI) || kk != 0) ? 1u : 0u;
             umma_f16_ts(d0, tA + kk * 8, bdesc, idesc, acc);
-            if (C::NA == 2) umma_f16_ts(d0 + BN, tA + 32 + kk * 8, bdesc, idesc, acc);
+            if (C::NA == 2 && !OPS) umma_f16_ts(d0 + BN, tA + 32 + kk * 8, bdesc, idesc, acc);
           }
           umma_commit(t_empty(ts));
-          umma_commit(conv_empty(cs));
+          umma_commit(conv_empty(cs, cb));
         }
         if (!ok) break;
         umma_commit(accf0 + 8u * buf);
@@ -320,7 +348,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
     }
   } else if (warp < kFirstConvWarp) {
     // ------------------------------------------------------------ epilogue (warps 3..10)
-    tc::epilogue_loop<MODE, BN, C::NACC, C::NBUF, true, NI>(p, total, m_tiles, KB, prefix,
+    tc::epilogue_loop<MODE, BN, C::NACC, C::NBUF, true, C::NPART>(p, total, m_tiles, KB, prefix,
                                                             gstart, tmem_base, accf0, acce0,
                                                             abort_flag, kFirstEpiWarp,
                                                             blockIdx.x, gridDim.x, 0);
@@ -339,6 +367,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
     const int cw = warp - kFirstConvWarp;
     const int q = warp & 3, r = q * 32 + lane;
     const int op = C::NA == 2 ? cw >> 2 : 0;
+    const int cb = OPS ? op : 0;  // converted-stage barriers this warp uses
     const uint32_t group = C::NA == 2 ? 0u : (uint32_t)(cw >> 2);  // down: stage parity
     const int swz = r & 7;  // 128-byte swizzle: chunk j of code row r sits at j ^ (r % 8)
     const int code_off = op * C::QA_BYTES + r * 128;
@@ -383,7 +412,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
         for (int h = 0; h < 2; ++h) {
           if (h >= nk) break;
           const int cs = kcount % CS;
-          if (!tc::mbar_wait_warp(conv_empty(cs), ((kcount / CS) & 1u) ^ 1u, abort_flag,
+          if (!tc::mbar_wait_warp(conv_empty(cs, cb), ((kcount / CS) & 1u) ^ 1u, abort_flag,
                                   p.err)) {
             ok = false;
             break;
@@ -409,7 +438,7 @@ __global__ void __launch_bounds__(threads_q8(NI), 1)
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(conv_full(cs));
+          if (lane == 0) mbar_arrive(conv_full(cs, cb));
           ++kcount;
           if (h == 0) hand_back();
         }
@@ -442,12 +471,12 @@ bool make_q8_maps(CUtensorMap* tq, CUtensorMap* ts, const Q8Weight& w, int n_gro
                       (uint64_t)n_groups * (K / 32), 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-template <int MODE, int BN, int WS, int TS, int CS, int NI>
+template <int MODE, int BN, int WS, int TS, int CS, int NI, bool OPS = false>
 cudaError_t launch_q8(const CUtensorMap& q0, const CUtensorMap& q1, const CUtensorMap& s0,
                       const CUtensorMap& s1, const CUtensorMap& b, const CUtensorMap& bfull,
                       const Params& p, long long max_units, const char* name, cudaStream_t s) {
-  using C = CfgQ8<MODE, BN, WS, TS, CS, NI>;
-  auto kern = tc_grouped_gemm_q8<MODE, BN, WS, TS, CS, NI>;
+  using C = CfgQ8<MODE, BN, WS, TS, CS, NI, OPS>;
+  auto kern = tc_grouped_gemm_q8<MODE, BN, WS, TS, CS, NI, OPS>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -493,7 +522,7 @@ cudaError_t launch_ffn_tc_q8(const void* x_perm, const int32_t* offsets, int n_g
   const char* n1 = "ffn_gateup_tc_q8";
   const cudaError_t e =
       small ? launch_q8<MODE_GATEUP, 32, 5, 8, 4, 2>(qg, qu, sg, su, tx, txf, p1, u1, n1, s)
-            : launch_q8<MODE_GATEUP, 192, 3, 4, 2, 1>(qg, qu, sg, su, tx, txf, p1, u1, n1, s);
+            : launch_q8<MODE_GATEUP, 192, 3, 4, 2, 2, true>(qg, qu, sg, su, tx, txf, p1, u1, n1, s);
   if (e != cudaSuccess) return e;
   Params p2{offsets, n_groups, 0, d, I, y_perm, d, slot_w, err, P};
   const long long u2 = (long long)((d + 127) / 128) * ((P + bn2 - 1) / bn2 + n_groups);
