@@ -555,6 +555,76 @@ def host_huge_fraction(nbytes):
     return None
 
 
+_MOVE_PAGES = {"x86_64": 279, "aarch64": 239}
+
+
+def host_pages_numa(tensors, samples=256):
+    """Share of sampled pages of the tensors' host memory on each NUMA node
+    (Linux move_pages query, nodes not given: nothing moves), or None."""
+    nr = _MOVE_PAGES.get(os.uname().machine)
+    if nr is None:
+        return None
+    try:
+        import ctypes
+        libc = ctypes.CDLL(None, use_errno=True)
+        page = os.sysconf("SC_PAGE_SIZE")
+        addrs = []
+        for t in tensors:
+            base, n = t.data_ptr(), t.numel() * t.element_size()
+            k = max(1, samples // len(tensors))
+            addrs += [(base + (n - 1) * i // max(1, k - 1)) // page * page for i in range(k)]
+        pages = (ctypes.c_void_p * len(addrs))(*addrs)
+        status = (ctypes.c_int * len(addrs))()
+        if libc.syscall(nr, 0, ctypes.c_ulong(len(addrs)), pages, None, status, 0) != 0:
+            return None
+        count = {}
+        for v in status:
+            key = str(v) if v >= 0 else "error"
+            count[key] = count.get(key, 0) + 1
+        return {k: c / len(addrs) for k, c in sorted(count.items())}
+    except (OSError, AttributeError, ValueError):
+        return None
+
+
+def cpu_numa_nodes():
+    """NUMA nodes of the CPUs this process may run on (Linux), or None."""
+    try:
+        allowed = os.sched_getaffinity(0)
+        nodes = []
+        root = "/sys/devices/system/node"
+        for name in sorted(os.listdir(root)):
+            if not name.startswith("node") or not name[4:].isdigit():
+                continue
+            with open(os.path.join(root, name, "cpulist")) as f:
+                spec = f.read().strip()
+            cpus = set()
+            for part in filter(None, spec.split(",")):
+                lo, _, hi = part.partition("-")
+                cpus.update(range(int(lo), int(hi or lo) + 1))
+            if cpus & allowed:
+                nodes.append(int(name[4:]))
+        return nodes
+    except (OSError, AttributeError, ValueError):
+        return None
+
+
+def tier_memory_copy_gbs(h, dev, n_bytes=1 << 30, reps=3):
+    """Copy-engine rate (GB/s, best of reps) reading the tier's own host weights:
+    the same memory the load kernel reads, through the other mechanism."""
+    src = h.view(-1).view(torch.uint8)[:n_bytes]
+    d = torch.empty(src.numel(), dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(reps + 1):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        d.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, src.numel() / (a.elapsed_time(b) / 1e3) / 1e9)
+    del d
+    return best
+
+
 def percentiles(v):
     """min / p10 / median / p90 / max of a list (None when empty)."""
     if not v:
@@ -629,6 +699,7 @@ def run_tier(args, rank, world):
     timed(lambda x: layer.forward(x, y=y), args.warmup)
     resident_ms = timed(lambda x: layer.forward(x, y=y), args.steps)
     link = host_link_gbs(dev)
+    tier_copy = tier_memory_copy_gbs(host_w[0], dev)
     touch = None
     if args.tier_touch:  # read every expert's host memory from the GPU once, untimed
         nE = cfg.E + cfg.S
@@ -671,6 +742,7 @@ def run_tier(args, rank, world):
             stream.synchronize()
             step_ms.append((time.perf_counter() - t0) * 1e3)
     link_after = host_link_gbs(dev)
+    tier_copy_after = tier_memory_copy_gbs(host_w[0], dev)
     loads = load_summary(timed_ms, timed_bytes)
     loaded = d["bytes_loaded"] / K
     bound_ms = resident_ms / K + loaded / (link * 1e9) * 1e3
@@ -696,6 +768,12 @@ def run_tier(args, rank, world):
                  "h2d_gbs_achieved": d["bytes_loaded"] / (ms / 1e3) / 1e9,
                  "host_weights_in_huge_pages": huge,
                  "host_link_gbs_after": link_after,
+                 # where the host weights sit, and a copy-engine read of that very
+                 # memory before / after the timed region (the link figures above
+                 # read a separate page-locked buffer)
+                 "host_weights_numa": host_pages_numa(host_w),
+                 "process_cpu_numa_nodes": cpu_numa_nodes(),
+                 "tier_memory_copy_gbs": [tier_copy, tier_copy_after],
                  "loads_in_timed_region": loads,
                  "host_memory_touched_first": touch,
                  "repeat_step_wall_ms": percentiles(step_ms)},
