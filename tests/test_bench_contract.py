@@ -129,3 +129,19 @@ def test_source_hash_ignores_comments_only():
     c = "int f(int x) { return 3 * x; }"
     assert bench._code_only(a) == bench._code_only(b)
     assert bench._code_only(a) != bench._code_only(c)
+
+
+def test_tier_record_host_memory_queries():
+    # the tier record's placement fields: the sampled pages' NUMA nodes (shares
+    # summing to one) and the nodes of the CPUs this process may run on
+    import torch
+
+    bench = _bench()
+    ts = [torch.ones(1 << 20, dtype=torch.uint8), torch.ones(1 << 18, dtype=torch.bfloat16)]
+    numa = bench.host_pages_numa(ts, samples=16)
+    nodes = bench.cpu_numa_nodes()
+    if not sys.platform.startswith("linux") or numa is None or nodes is None:
+        pytest.skip("no NUMA query here")
+    assert abs(sum(numa.values()) - 1.0) < 1e-9
+    assert "error" not in numa
+    assert nodes and all(isinstance(n, int) and n >= 0 for n in nodes)
