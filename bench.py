@@ -375,9 +375,18 @@ def measure_workload(cfg, args, weights, rank, world, dev, cpu_budget=None):
     # ---- end to end: the C-ABI call a serving loop makes with host buffers
     # (moe_layer_forward_host_pipelined): every step, pinned host x -> device,
     # the layer, device y -> pinned host; the copies of neighbouring steps overlap
-    # the compute.  Two pinned x and two pinned y buffers, used in turn.
-    x_ring = [x.cpu().pin_memory() for _ in range(2)]
-    y_ring = [torch.empty((cfg.T, cfg.d), dtype=torch.float32).pin_memory() for _ in range(2)]
+    # the compute.  Two pinned x and two pinned y buffers, used in turn.  Buffers of
+    # 64 MB and more come from the library's host allocator (huge pages, page-locked:
+    # large copies from base-page pinned memory ran at about half the link's rate).
+    big = cfg.T * cfg.d * 4 >= 64 << 20
+
+    def pinned(shape, dtype):
+        return moe.host_empty(shape, dtype) if big else torch.empty(shape, dtype=dtype).pin_memory()
+
+    x_ring = [pinned((cfg.T, cfg.d), x.dtype) for _ in range(2)]
+    for h in x_ring:
+        h.copy_(x)
+    y_ring = [pinned((cfg.T, cfg.d), torch.float32) for _ in range(2)]
 
     def host_run(n):
         layer.forward_host_pipelined([x_ring[i % 2] for i in range(n)],
